@@ -1,0 +1,392 @@
+#!/usr/bin/env python
+"""Benchmark of the K3 DFlash drafter block attention; prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload long_context|mixed_8x8|heads_24_4|tiny]
+
+Metric: drafter block-attention microseconds per call (lower is better) on
+one of the op's workloads, default the long-context one (8 requests x 8 draft
+tokens, 24/4 heads, contexts U{16384..131072}, a 20,000-page bf16 pool,
+fused RMSNorm + RoPE, int64 positions), with the achieved HBM bandwidth of
+the dominant kernel against the measured copy bandwidth in "roofline".
+
+ours:       the CUDA library through its Python binding.  Inputs are resident
+            in HBM; L2 is flushed (512 MB write) before every timed call; each
+            call is timed with CUDA events on the launching stream.
+            "e2e" times the same call with the per-step inputs (qkv, page
+            table, lengths, positions) copied from pinned host memory and the
+            output copied back, inside the timed region.
+reference:  the fp64 CPU oracle (test infrastructure, timed as it stands on
+            the host cores), each step a bounded sample of the same workload
+            scaled to a whole call.
+
+Multi-GPU: the op does not shard across GPUs in a way that needs any
+exchange; N ranks run N independent replicas ("replicas only") and value is
+the job's aggregate time per call (max-over-ranks time / calls of all ranks).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "drafter block-attn µs/call and HBM GB/s (% of GB300 peak) at 8 req × 8 tok"
+UNIT = "us/call"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCE = os.path.join(ROOT, "speculative_decoding_drafter_k3_gb300", "csrc", "k3da.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="long_context")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            data = json.load(open(path))
+
+            def find(d):
+                if isinstance(d, dict):
+                    for k, v in d.items():
+                        if k == "hbm_gbs" and isinstance(v, (int, float)):
+                            return float(v)
+                        r = find(v)
+                        if r:
+                            return r
+                return None
+
+            v = find(data)
+            if v:
+                return v, "measured (MEASURED_PEAKS.json hbm_gbs)"
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 copy measurement)"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={device_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_source_hash() -> str:
+    return hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the split kernel from a committed ncu capture,
+    or None when absent or taken on a different kernel source."""
+    try:
+        data = json.load(open(PROFILE_TRAFFIC))
+    except (OSError, ValueError):
+        return None
+    entry = data.get(workload)
+    if not entry or entry.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------- CPU oracle --
+
+def compact_request(case, r):
+    """Request r alone, with its pool reduced to the pages it reads (input
+    marshalling only), on the CPU."""
+    from speculative_decoding_drafter_k3_gb300 import workloads
+
+    sub = case.request(r)
+    L = sub.lens_list()[0]
+    n = (L + workloads.PAGE_SIZE - 1) // workloads.PAGE_SIZE
+    pages = sub.page_table[0, :n].long()
+    pool = case.pool[pages.to(case.pool.device)].cpu() if n else case.pool[:1].cpu()
+    pt = torch.full((1, max(n, 1)), -1, dtype=torch.int32)
+    pt[0, :n] = torch.arange(n, dtype=torch.int32)
+    sub.pool, sub.page_table, sub.num_pages = pool, pt, pool.shape[0]
+    return sub.to("cpu")
+
+
+def oracle_seconds(sub) -> float:
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.attn(sub.qkv, sub.pool, sub.page_table, sub.ctx_lens, num_requests=1, block_len=sub.B,
+                num_q_heads=sub.Hq, num_kv_heads=sub.Hkv, scale=sub.scale, qknorm=sub.qknorm,
+                positions=sub.positions, q_norm_w=sub.q_norm_w, k_norm_w=sub.k_norm_w,
+                eps=sub.eps, rope_base=sub.rope_base)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(case, budget_s: float = 12.0):
+    """Oracle on requests in ascending context length until ~budget_s of CPU
+    work, scaled to one call by (context + block) tokens."""
+    import oracle
+
+    oracle.build()
+    lens = case.lens_list()
+    order = sorted(range(case.R), key=lambda r: lens[r])
+    spent, tokens, used = 0.0, 0, []
+    for r in order:
+        spent += oracle_seconds(compact_request(case, r))
+        tokens += lens[r] + case.B
+        used.append(r)
+        if spent >= budget_s:
+            break
+    total = sum(L + case.B for L in lens)
+    us_per_call = spent * total / tokens * 1e6
+    return {"value": us_per_call, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": (f"fp64 C oracle, 1 thread, on requests {used} of {case.R} "
+                       f"({tokens} of {total} context+block tokens, {spent:.1f} s), "
+                       f"scaled to one call by token count")}
+
+
+# ------------------------------------------------------------------ arms --
+
+def config_of(case, extra=None):
+    cfg = {"workload": case.name, "requests": case.R, "block_tokens": case.B,
+           "heads": f"{case.Hq}/{case.Hkv}", "head_dim": case.D, "page_size": case.P,
+           "pool_pages": case.num_pages, "page_stride": case.page_stride,
+           "qknorm_rope": case.qknorm, "positions": str(case.pos_dtype).replace("torch.", ""),
+           "context_tokens": case.context_tokens(), "ctx_lens": case.lens_list(),
+           "algorithmic_bytes_per_call": case.algorithmic_bytes(),
+           "l2": "flushed before every timed call (512 MB write)"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def run_reference(args, world, rank):
+    from speculative_decoding_drafter_k3_gb300 import workloads
+    import oracle
+
+    if rank != 0:
+        return
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    case = workloads.WORKLOADS[args.workload](device=dev)
+    oracle.build()
+    lens = case.lens_list()
+    r = min(range(case.R), key=lambda i: lens[i])
+    sub = compact_request(case, r)
+    scale = sum(L + case.B for L in lens) / (lens[r] + case.B)
+    for _ in range(args.warmup):
+        oracle_seconds(sub)
+    times = [oracle_seconds(sub) * scale for _ in range(args.steps)]
+    us = statistics.mean(times) * 1e6
+    sample = (f"fp64 C oracle, 1 thread, request {r} of {case.R} ({lens[r]}+{case.B} tokens) per "
+              f"step, scaled to one call by context+block tokens (x{scale:.2f})")
+    line = {"impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(case),
+            "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank):
+    import speculative_decoding_drafter_k3_gb300 as k3da
+    from speculative_decoding_drafter_k3_gb300 import build as kbuild, workloads
+
+    kbuild.build()
+    k3da.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = workloads.WORKLOADS[args.workload](device=dev)
+    out = torch.empty(case.T, case.Hq * case.D, dtype=torch.bfloat16, device=dev)
+    ws = k3da.alloc_workspace(case.R, case.B, case.Hq, case.Hkv, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def call():
+        k3da.run_case(case, out=out, workspace=ws, status=status)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record()
+        k3da.set_phase_event(ev[i][1])
+        call()
+        ev[i][2].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    k3da.set_phase_event(None)
+    clock_info = clocks.stop() if clocks else None
+    call_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    split_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    total_ms = max_over_ranks(sum(call_ms), world)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    value = total_ms * 1e3 / (K * world)
+
+    # End to end through the public binding with host buffers.
+    e2e = None
+    if not args.no_e2e:
+        inputs = [case.qkv, case.page_table, case.ctx_lens] + ([case.positions] if case.qknorm else [])
+        host_in = [t.cpu().pin_memory() for t in inputs]
+        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        for _ in range(3):
+            for d, h in zip(inputs, host_in):
+                d.copy_(h, non_blocking=True)
+            call()
+            host_out.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        eev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush.zero_()
+            eev[i][0].record()
+            for d, h in zip(inputs, host_in):
+                d.copy_(h, non_blocking=True)
+            call()
+            host_out.copy_(out, non_blocking=True)
+            eev[i][1].record()
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in eev), world)
+        e2e = {"value": e2e_ms * 1e3 / (K * world), "unit": UNIT,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in inputs),
+               "d2h_bytes_per_step": out.numel() * out.element_size()}
+
+    out_bytes = case.T * case.Hq * case.D * 2
+    split_bytes = case.algorithmic_bytes() - out_bytes
+    split_us = statistics.mean(split_ms) * 1e3
+    peak, peak_src = measured_hbm_peak()
+    achieved = split_bytes / (split_us * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
+                "kernel": "k3da_split_kernel (split pass; combine excluded)",
+                "algorithmic_bytes_per_launch": split_bytes, "launch_us": split_us,
+                "peak_source": peak_src,
+                "whole_call_gbs": case.algorithmic_bytes() / (value * 1e-6) / 1e9}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",
+            "data": "synthetic (seeded N(0,1) bf16 pool/qkv, random page permutation)",
+            "config": config_of(case, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
+            "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clock_info,
+            "median_call_us": statistics.median(call_ms) * 1e3,
+            "p10_p90_call_us": [sorted(call_ms)[int(0.1 * (K - 1))] * 1e3,
+                                sorted(call_ms)[int(0.9 * (K - 1))] * 1e3]}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

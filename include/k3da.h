@@ -1,0 +1,154 @@
+/*
+ * k3da.h -- C ABI of the K3 DFlash drafter block attention for sm_103a.
+ *
+ * The operation is the one the page "[None][feat] Share Kimi K3 FP4 modeling
+ * and add NVFP4 support on SM103" (NVIDIA/TensorRT-LLM PR #20532) defines in
+ * the commit adding the ops k3_drafter_attn and k3_drafter_attn_qknorm, with
+ * the parameters fixed by the commit adding their contracts and the
+ * drafter's fused_qk_norm_rope cell:
+ *
+ *   Each of R <= 8 requests brings a draft block of B <= 8 tokens.  Every
+ *   block token attends densely (non-causally) to its request's paged
+ *   context and to the K/V of its own block.  The block K/V are read from
+ *   qkv and never written to the pool.  GQA with 6 query heads per KV head
+ *   (head layouts 6/1 and 24/4), head_dim 64, HND pages of 64 tokens.
+ *   k3da_attn takes q and k already normalised and roped; k3da_attn_qknorm
+ *   applies the per-head q/k RMSNorm and the NeoX RoPE itself.
+ *
+ * Notation: T = R*B rows, Hq query heads, Hkv KV heads, D = 64, P = 64
+ * tokens per page, S = page stride (entries per page-table row), G = Hq/Hkv.
+ *
+ * Memory.  Every pointer is DEVICE memory owned by the caller, except where
+ * a comment says otherwise.  The library allocates nothing, keeps no
+ * per-call state, never synchronises and never reads device data on the
+ * host: lengths, page table, positions and qkv are read by the kernels, so a
+ * call captured in a CUDA graph replays with those buffers rewritten.  The
+ * first call on a device (which configures the kernels for it) should come
+ * before any stream capture.  The KV pool is only read.
+ *
+ * Errors.  A host-side check that fails returns a negative k3da_error
+ * before anything is launched and nothing is written.  Checks that need
+ * device data (lengths, page ids) are made by the kernels: a violation is
+ * OR-ed into *status as a K3DA_STATUS_* bit, the offending read is skipped
+ * (a clamped length, a page of zeros) and the output stays finite.  The
+ * kernels never trap.
+ */
+#ifndef K3DA_H
+#define K3DA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes (host-side). */
+typedef enum {
+    K3DA_OK = 0,
+    K3DA_EINVAL = -1,       /* NULL or misaligned pointer, size out of range */
+    K3DA_EUNSUPPORTED = -2, /* head layout, head_dim or page size not served */
+    K3DA_ECUDA = -3,        /* a CUDA runtime call failed (launch, attribute) */
+    K3DA_EWORKSPACE = -4    /* workspace NULL or smaller than k3da_workspace_bytes */
+} k3da_error;
+
+/* Bits OR-ed into the device status word by the kernels. */
+enum {
+    K3DA_STATUS_BAD_LENGTH = 1, /* ctx_len < 0 or > page_stride*64: clamped */
+    K3DA_STATUS_BAD_PAGE = 2,   /* page id outside [0, num_pages): zeros used */
+    K3DA_STATUS_TIMEOUT = 4     /* an internal wait ran out: output invalid */
+};
+
+/* Integer type of the positions array. */
+typedef enum { K3DA_POS_I32 = 0, K3DA_POS_I64 = 1 } k3da_pos_dtype;
+
+/*
+ * Bytes of device workspace a call with these sizes needs on `device`
+ * (-1 = the current device).  Returns 0 when the sizes are out of contract
+ * or the device cannot be queried.  The value depends on the device's SM
+ * count, not on lengths, so one buffer serves every call of a graph.
+ */
+size_t k3da_workspace_bytes(int num_requests, int block_len, int num_q_heads,
+                            int num_kv_heads, int device);
+
+/*
+ * k3da_attn -- block attention on already normalised and roped q / k
+ * (the op k3_drafter_attn of the commit named above).
+ *
+ *   out          [T, Hq*64] bf16, written.  16-byte aligned.
+ *   qkv          [T, (Hq + 2*Hkv)*64] bf16.  Row r*B + i is token i of
+ *                request r: Hq query heads, then Hkv key heads, then Hkv
+ *                value heads, 64 dims each.  16-byte aligned.
+ *   kv_pool      [num_pages, 2, Hkv, 64, 64] bf16; [page][K=0,V=1][kv head]
+ *                [slot][dim].  Read only.  16-byte aligned.
+ *   num_pages    pages in the pool, >= 1, num_pages*2*Hkv*64 < 2^31.
+ *   page_table   [R, page_stride] int32; context token c of request r is in
+ *                page page_table[r*page_stride + c/64], slot c%64.  Entries
+ *                past ceil(ctx_len/64) are never read.
+ *   page_stride  entries per page-table row, >= 1.
+ *   ctx_lens     [R] int32 context lengths, 0 <= len <= page_stride*64.
+ *   num_requests R in [1, 8];  block_len B in [1, 8].
+ *   num_q_heads, num_kv_heads   (6, 1) or (24, 4); query head h reads KV
+ *                head h / 6.
+ *   head_dim     64.
+ *   softmax_scale  multiplier of q.k (1/sqrt(64) for the drafter); finite, > 0.
+ *   workspace, workspace_bytes  scratch of at least k3da_workspace_bytes();
+ *                contents on entry are irrelevant; 16-byte aligned.
+ *   status       int32 device word the kernels OR K3DA_STATUS_* bits into;
+ *                may be NULL.  The caller clears it.
+ *   stream       cudaStream_t to launch on (NULL = legacy default stream).
+ *
+ * Returns K3DA_OK once both kernels are enqueued, else a k3da_error.
+ * Calls on the same stream are ordered; calls that share a workspace must
+ * not overlap on the GPU.
+ */
+int k3da_attn(void *out, const void *qkv, const void *kv_pool, int64_t num_pages,
+              const int32_t *page_table, int page_stride, const int32_t *ctx_lens,
+              int num_requests, int block_len, int num_q_heads, int num_kv_heads,
+              int head_dim, float softmax_scale, void *workspace, size_t workspace_bytes,
+              int32_t *status, void *stream);
+
+/*
+ * k3da_attn_qknorm -- as k3da_attn, but q and the block's k are raw: each
+ * 64-wide head row x of q (resp. k) becomes
+ *     y = x * (mean_j x_j^2 + eps)^(-1/2) * w      (w = q_norm_w, resp. k_norm_w)
+ * and then NeoX RoPE at the token's position p: for j < 32,
+ *     theta = p * rope_base^(-2j/64),
+ *     y'_j = y_j cos(theta) - y_{j+32} sin(theta),
+ *     y'_{j+32} = y_{j+32} cos(theta) + y_j sin(theta).
+ * Context keys in the pool are used as stored; values are never normalised
+ * (the op k3_drafter_attn_qknorm of the commit named above; eps 1e-5 and
+ * base 10000 in its fused_qk_norm_rope cell).
+ *
+ *   positions    [T] int32 or int64 (pos_dtype), 0 <= p < 2^24 for exact
+ *                angles; 4- or 8-byte aligned.
+ *   q_norm_w, k_norm_w   [64] bf16 RMSNorm weights shared by all heads.
+ *   eps          >= 0, finite;  rope_base > 1, finite.
+ */
+int k3da_attn_qknorm(void *out, const void *qkv, const void *kv_pool, int64_t num_pages,
+                     const int32_t *page_table, int page_stride, const int32_t *ctx_lens,
+                     int num_requests, int block_len, int num_q_heads, int num_kv_heads,
+                     int head_dim, float softmax_scale, const void *positions,
+                     int pos_dtype, const void *q_norm_w, const void *k_norm_w, float eps,
+                     float rope_base, void *workspace, size_t workspace_bytes,
+                     int32_t *status, void *stream);
+
+/*
+ * Profiling aid.  When `event` (a cudaEvent_t created by the caller) is not
+ * NULL, every later k3da_attn / k3da_attn_qknorm call made from this host
+ * thread records it on the call's stream between the split pass and the
+ * combine kernel, so the split pass can be timed alone; NULL turns this off.
+ * The setting is per host thread.  Returns K3DA_OK.
+ */
+int k3da_set_phase_event(void *event);
+
+/* Static description of a k3da_error or K3DA_STATUS_* bit set. */
+const char *k3da_error_string(int code);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int k3da_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* K3DA_H */

@@ -1,0 +1,202 @@
+"""K3 DFlash drafter block attention on sm_103a: thin Python binding.
+
+The compute lives in ``libk3da.so`` (hand-written CUDA, C ABI declared in
+``include/k3da.h``).  This module only marshals torch tensors into that ABI:
+device pointers, sizes, dtype codes and the current CUDA stream.  There is no
+CPU fallback: if the library is missing, every call raises.
+
+Operation (page "[None][feat] Share Kimi K3 FP4 modeling and add NVFP4
+support on SM103", NVIDIA/TensorRT-LLM PR #20532, commit adding
+k3_drafter_attn / k3_drafter_attn_qknorm): each of R <= 8 requests brings a
+block of B <= 8 draft tokens; every block token attends densely to its
+request's paged context (HND pages of 64) and to its own block's K/V, taken
+from qkv and never written to the pool; GQA 6:1 (6/1 or 24/4 heads),
+head_dim 64.  ``k3da_attn_qknorm`` first applies per-head q/k RMSNorm and
+NeoX RoPE.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "K3daError", "library_path", "load_library", "workspace_bytes", "k3da_attn",
+    "k3da_attn_qknorm", "STATUS_BAD_LENGTH", "STATUS_BAD_PAGE", "STATUS_TIMEOUT",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libk3da.so")
+_lock = threading.Lock()
+_lib = None
+
+OK, EINVAL, EUNSUPPORTED, ECUDA, EWORKSPACE = 0, -1, -2, -3, -4
+STATUS_BAD_LENGTH, STATUS_BAD_PAGE, STATUS_TIMEOUT = 1, 2, 4
+POS_I32, POS_I64 = 0, 1
+EXPORTED = ["k3da_workspace_bytes", "k3da_attn", "k3da_attn_qknorm", "k3da_set_phase_event",
+            "k3da_error_string", "k3da_version"]
+
+
+class K3daError(ValueError):
+    """A call refused by the library (host-side check) or a device status."""
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libk3da.so (ctypes) and declare its signatures; raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with "
+                "`python -m speculative_decoding_drafter_k3_gb300.build` (there is no CPU fallback)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        c_int, c_i64, c_sz, vp, c_f = (ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
+                                       ctypes.c_void_p, ctypes.c_float)
+        lib.k3da_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int]
+        lib.k3da_workspace_bytes.restype = c_sz
+        common = [vp, vp, vp, c_i64, vp, c_int, vp, c_int, c_int, c_int, c_int, c_int, c_f]
+        lib.k3da_attn.argtypes = common + [vp, c_sz, vp, vp]
+        lib.k3da_attn.restype = c_int
+        lib.k3da_attn_qknorm.argtypes = common + [vp, c_int, vp, vp, c_f, c_f, vp, c_sz, vp, vp]
+        lib.k3da_attn_qknorm.restype = c_int
+        lib.k3da_error_string.argtypes = [c_int]
+        lib.k3da_error_string.restype = ctypes.c_char_p
+        lib.k3da_set_phase_event.argtypes = [vp]
+        lib.k3da_set_phase_event.restype = c_int
+        lib.k3da_version.argtypes = []
+        lib.k3da_version.restype = c_int
+        _lib = lib
+        return lib
+
+
+def error_string(code: int) -> str:
+    return load_library().k3da_error_string(int(code)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise K3daError(f"{what}: {error_string(rc)} (code {rc})")
+
+
+def workspace_bytes(num_requests: int, block_len: int, num_q_heads: int, num_kv_heads: int,
+                    device: int = -1) -> int:
+    n = load_library().k3da_workspace_bytes(num_requests, block_len, num_q_heads, num_kv_heads,
+                                            device)
+    if n == 0:
+        raise K3daError("workspace_bytes: sizes out of contract or device not queryable")
+    return int(n)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _shape_args(out, qkv, kv_pool, page_table, ctx_lens, block_len, num_q_heads, num_kv_heads):
+    for name, t in [("out", out), ("qkv", qkv), ("kv_pool", kv_pool), ("page_table", page_table),
+                    ("ctx_lens", ctx_lens)]:
+        if not t.is_cuda or not t.is_contiguous():
+            raise K3daError(f"{name} must be a contiguous CUDA tensor")
+    if qkv.dtype != torch.bfloat16 or out.dtype != torch.bfloat16 or kv_pool.dtype != torch.bfloat16:
+        raise K3daError("qkv, out and kv_pool must be bf16")
+    if page_table.dtype != torch.int32 or ctx_lens.dtype != torch.int32:
+        raise K3daError("page_table and ctx_lens must be int32")
+    if page_table.dim() != 2 or kv_pool.dim() != 5:
+        raise K3daError("page_table must be [R, S] and kv_pool [pages, 2, Hkv, 64, 64]")
+    R = page_table.shape[0]
+    T = R * block_len
+    D = kv_pool.shape[-1]
+    if (tuple(kv_pool.shape[1:]) != (2, num_kv_heads, 64, D) or ctx_lens.numel() != R
+            or tuple(qkv.shape) != (T, (num_q_heads + 2 * num_kv_heads) * D)
+            or tuple(out.shape) != (T, num_q_heads * D)):
+        raise K3daError("tensor shapes disagree with (R, B, Hq, Hkv, head_dim)")
+    return R, kv_pool.shape[0], page_table.shape[1], D
+
+
+def k3da_attn(out, qkv, kv_pool, page_table, ctx_lens, *, block_len: int, num_q_heads: int,
+              num_kv_heads: int, softmax_scale: float = 0.125, workspace, status=None,
+              stream=None):
+    """Block attention on already normalised and roped q/k (C: k3da_attn)."""
+    lib = load_library()
+    R, num_pages, S, D = _shape_args(out, qkv, kv_pool, page_table, ctx_lens, block_len,
+                                     num_q_heads, num_kv_heads)
+    rc = lib.k3da_attn(_ptr(out), _ptr(qkv), _ptr(kv_pool), num_pages, _ptr(page_table), S,
+                       _ptr(ctx_lens), R, block_len, num_q_heads, num_kv_heads, D,
+                       float(softmax_scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                       _ptr(status), _stream(stream))
+    _check(rc, "k3da_attn")
+    return out
+
+
+def k3da_attn_qknorm(out, qkv, kv_pool, page_table, ctx_lens, positions, q_norm_w, k_norm_w, *,
+                     block_len: int, num_q_heads: int, num_kv_heads: int,
+                     softmax_scale: float = 0.125, eps: float = 1e-5, rope_base: float = 10000.0,
+                     workspace, status=None, stream=None):
+    """Block attention with fused q/k RMSNorm + NeoX RoPE (C: k3da_attn_qknorm)."""
+    lib = load_library()
+    R, num_pages, S, D = _shape_args(out, qkv, kv_pool, page_table, ctx_lens, block_len,
+                                     num_q_heads, num_kv_heads)
+    if positions.dtype not in (torch.int32, torch.int64) or positions.numel() != R * block_len:
+        raise K3daError("positions must be [T] int32 or int64")
+    for name, t in [("positions", positions), ("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)]:
+        if not t.is_cuda or not t.is_contiguous():
+            raise K3daError(f"{name} must be a contiguous CUDA tensor")
+    if q_norm_w.dtype != torch.bfloat16 or k_norm_w.dtype != torch.bfloat16 or \
+            q_norm_w.numel() != D or k_norm_w.numel() != D:
+        raise K3daError("norm weights must be [64] bf16")
+    pos_code = POS_I64 if positions.dtype == torch.int64 else POS_I32
+    rc = lib.k3da_attn_qknorm(_ptr(out), _ptr(qkv), _ptr(kv_pool), num_pages, _ptr(page_table), S,
+                              _ptr(ctx_lens), R, block_len, num_q_heads, num_kv_heads, D,
+                              float(softmax_scale), _ptr(positions), pos_code, _ptr(q_norm_w),
+                              _ptr(k_norm_w), float(eps), float(rope_base), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _ptr(status),
+                              _stream(stream))
+    _check(rc, "k3da_attn_qknorm")
+    return out
+
+
+def alloc_workspace(num_requests: int, block_len: int, num_q_heads: int, num_kv_heads: int,
+                    device=None) -> torch.Tensor:
+    """A workspace tensor (uint8, 16-byte aligned) sized for these shapes."""
+    device = torch.device("cuda") if device is None else torch.device(device)
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    n = workspace_bytes(num_requests, block_len, num_q_heads, num_kv_heads, idx)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def run_case(case, out=None, workspace=None, status=None, stream=None):
+    """Run the op on a ``workloads.Case`` whose tensors are on the GPU."""
+    if out is None:
+        out = torch.empty(case.T, case.Hq * case.D, dtype=torch.bfloat16, device=case.qkv.device)
+    if workspace is None:
+        workspace = alloc_workspace(case.R, case.B, case.Hq, case.Hkv, case.qkv.device)
+    kw = dict(block_len=case.B, num_q_heads=case.Hq, num_kv_heads=case.Hkv,
+              softmax_scale=case.scale, workspace=workspace, status=status, stream=stream)
+    if case.qknorm:
+        return k3da_attn_qknorm(out, case.qkv, case.pool, case.page_table, case.ctx_lens,
+                                case.positions, case.q_norm_w, case.k_norm_w, eps=case.eps,
+                                rope_base=case.rope_base, **kw)
+    return k3da_attn(out, case.qkv, case.pool, case.page_table, case.ctx_lens, **kw)
+
+
+def set_phase_event(event):
+    """Record ``event`` (a torch.cuda.Event) between the split pass and the
+    combine of every later call from this thread; None turns it off."""
+    if event is None:
+        handle = None
+    else:
+        handle = ctypes.c_void_p(event.cuda_event)
+    _check(load_library().k3da_set_phase_event(handle), "k3da_set_phase_event")

@@ -1,0 +1,95 @@
+"""Parity of the CUDA path with the fp64 oracle, element by element, on the
+five workloads of the drafter block attention (6/1 and 24/4 heads, every
+request x token split, context lengths 0..2041 and 16k..128k, dense and
+strided page-table rows, int32 and int64 positions), plus edge cases.
+Tolerance: |gpu - oracle| <= 2e-2 + 2e-2 |oracle| on the bf16 output."""
+import numpy as np
+import pytest
+import torch
+
+import speculative_decoding_drafter_k3_gb300 as k3da
+from speculative_decoding_drafter_k3_gb300 import workloads
+from common import assert_close, oracle_for
+
+pytestmark = pytest.mark.gpu
+
+
+def run(case, **kw):
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = k3da.run_case(case, status=status, **kw)
+    torch.cuda.synchronize()
+    return out, int(status.item())
+
+
+def check(case):
+    out, st = run(case)
+    assert st == 0, f"{case.name}: device status {st}"
+    return assert_close(out, oracle_for(case), case.name)
+
+
+def test_tiny_plain_variant():
+    check(workloads.tiny(device="cuda"))
+
+
+def test_mixed_lengths_8x8_6_1_int32():
+    check(workloads.mixed_8x8(device="cuda"))
+
+
+def test_heads_24_4_strided_rows_int64():
+    check(workloads.heads_24_4(device="cuda"))
+
+
+@pytest.mark.parametrize("R,B", workloads.SPLITS)
+def test_split_sweep(R, B):
+    check(workloads.split_sweep(R, B, device="cuda"))
+
+
+@pytest.mark.parametrize("R,B", [(8, 8), (3, 5)])
+def test_split_sweep_plain_variant(R, B):
+    case = workloads.split_sweep(R, B, device="cuda", seed=50)
+    case.qknorm = False
+    check(case)
+
+
+@pytest.mark.parametrize("lens", [
+    [0] * 8,                          # block-only attention everywhere
+    [1, 63, 64, 65, 127, 128, 129, 2048],  # page boundaries, full row
+    [2048] * 8,                       # every page-table entry used
+])
+@pytest.mark.parametrize("Hq,Hkv", [(6, 1), (24, 4)])
+def test_edge_lengths(lens, Hq, Hkv):
+    case = workloads.build_case("edge", R=8, B=8, Hq=Hq, Hkv=Hkv, lens=lens, page_stride=32,
+                                num_pages=512, qknorm=True, pos_dtype=torch.int64, seed=60,
+                                device="cuda")
+    check(case)
+
+
+def test_single_token_single_request():
+    case = workloads.build_case("1x1", R=1, B=1, Hq=24, Hkv=4, lens=[777], page_stride=13,
+                                num_pages=40, qknorm=True, seed=61, device="cuda")
+    check(case)
+
+
+def test_large_positions_keep_rope_angles_exact():
+    # Positions near 131k: the RoPE angle must not lose precision.
+    case = workloads.build_case("bigpos", R=2, B=8, Hq=6, Hkv=1, lens=[100, 5], page_stride=4,
+                                num_pages=16, qknorm=True, pos_dtype=torch.int64, seed=62,
+                                device="cuda")
+    case.positions = case.positions + 131000
+    check(case)
+
+
+def test_long_context_sampled_requests():
+    """The long-context workload at full size (20k-page pool, 16k..128k
+    contexts, 24/4 heads), in the launch configuration the benchmark uses;
+    requests are independent, so the oracle checks two of them one by one."""
+    case = workloads.long_context(device="cuda")
+    out, st = run(case)
+    assert st == 0
+    lens = case.lens_list()
+    pool_cpu = case.pool.cpu()
+    for r in sorted({int(np.argmin(lens)), int(np.argmax(lens))}):
+        sub = case.request(r)
+        sub.pool = pool_cpu
+        ref = oracle_for(sub)
+        assert_close(out[r * case.B:(r + 1) * case.B], ref, f"long r{r} L={lens[r]}")

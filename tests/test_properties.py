@@ -1,0 +1,139 @@
+"""Properties the pages' tests ask of the op beyond parity: no NaN, the pool
+left byte-untouched, bit-identical reruns, isolated requests, device-side
+range checks that flag and never fault, a poisoned workspace, poisoned
+page-table tails and pool slots, and CUDA-graph replay with rewritten
+lengths, page table, qkv and positions."""
+import numpy as np
+import pytest
+import torch
+
+import speculative_decoding_drafter_k3_gb300 as k3da
+from speculative_decoding_drafter_k3_gb300 import workloads
+from common import assert_close, oracle_for
+
+pytestmark = pytest.mark.gpu
+
+
+def fresh_out(case):
+    return torch.empty(case.T, case.Hq * case.D, dtype=torch.bfloat16, device="cuda")
+
+
+def test_reruns_are_bit_identical_and_pool_untouched():
+    case = workloads.heads_24_4(device="cuda")
+    pool_before = case.pool.clone()
+    ws = k3da.alloc_workspace(case.R, case.B, case.Hq, case.Hkv)
+    a = k3da.run_case(case, workspace=ws).clone()
+    for _ in range(5):
+        ws.fill_(0xFF)  # NaN-pattern workspace between calls
+        b = k3da.run_case(case, workspace=ws)
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    torch.cuda.synchronize()
+    assert torch.equal(case.pool.view(torch.int16), pool_before.view(torch.int16))
+    assert torch.isfinite(a.float()).all()
+
+
+def test_requests_are_isolated():
+    case = workloads.mixed_8x8(device="cuda")
+    base = k3da.run_case(case).clone()
+    j = 3
+    other = workloads.mixed_8x8(device="cuda")
+    # Rewrite everything request j owns: its qkv rows, length, page row, positions.
+    rows = slice(j * case.B, (j + 1) * case.B)
+    case.qkv[rows] = torch.randn_like(case.qkv[rows].float()).to(torch.bfloat16)
+    case.ctx_lens[j] = 1999
+    case.page_table[j] = torch.flip(case.page_table[j], [0])
+    case.positions[rows] += 7
+    out = k3da.run_case(case)
+    torch.cuda.synchronize()
+    for r in range(case.R):
+        sl = slice(r * case.B, (r + 1) * case.B)
+        if r != j:
+            assert torch.equal(out[sl].view(torch.int16), base[sl].view(torch.int16)), r
+    assert_close(out, oracle_for(case), "isolation")
+    del other
+
+
+def test_poisoned_tails_and_stale_slots_are_never_used():
+    case = workloads.build_case("poison", R=4, B=8, Hq=6, Hkv=1, lens=[65, 100, 0, 129],
+                                page_stride=8, num_pages=64, qknorm=True, seed=70, device="cuda")
+    ref = oracle_for(case)
+    lens = case.lens_list()
+    nan = torch.tensor(float("nan"), dtype=torch.bfloat16, device="cuda")
+    used = set()
+    for r, L in enumerate(lens):
+        n = (L + 63) // 64
+        case.page_table[r, n:] = -1 if r % 2 else 10 ** 6  # past the context: never read
+        for p in range(n):
+            page = int(case.page_table[r, p])
+            used.add(page)
+            if p == n - 1 and L % 64:
+                case.pool[page, :, :, L % 64:, :] = nan  # stale slots after the context
+    for page in range(case.num_pages):
+        if page not in used:
+            case.pool[page] = nan
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = k3da.run_case(case, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_close(out, ref, "poisoned")
+
+
+def test_device_range_checks_flag_and_stay_finite():
+    case = workloads.build_case("bad", R=2, B=4, Hq=6, Hkv=1, lens=[100, 50], page_stride=2,
+                                num_pages=8, qknorm=True, seed=71, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    case.page_table[0, 1] = 8  # one past the pool
+    out = k3da.run_case(case, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & k3da.STATUS_BAD_PAGE
+    assert torch.isfinite(out.float()).all()
+    case.page_table[0, 1] = 1
+    case.ctx_lens[1] = 129  # beyond page_stride * 64
+    status.zero_()
+    out = k3da.run_case(case, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & k3da.STATUS_BAD_LENGTH
+    assert torch.isfinite(out.float()).all()
+    case.ctx_lens[1] = -5
+    status.zero_()
+    out = k3da.run_case(case, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & k3da.STATUS_BAD_LENGTH
+    assert torch.isfinite(out.float()).all()
+
+
+def test_host_side_refusals_raise():
+    case = workloads.tiny(device="cuda")
+    ws = k3da.alloc_workspace(case.R, case.B, case.Hq, case.Hkv)
+    with pytest.raises(k3da.K3daError):
+        k3da.run_case(case, workspace=ws[:16])  # too small
+    with pytest.raises(k3da.K3daError):
+        k3da.k3da_attn(fresh_out(case), case.qkv, case.pool, case.page_table, case.ctx_lens,
+                       block_len=case.B, num_q_heads=8, num_kv_heads=1, workspace=ws)
+
+
+@pytest.mark.parametrize("maker", [workloads.mixed_8x8, workloads.heads_24_4])
+def test_graph_replay_with_rewritten_inputs(maker):
+    case = maker(device="cuda")
+    ws = k3da.alloc_workspace(case.R, case.B, case.Hq, case.Hkv)
+    out = fresh_out(case)
+    k3da.run_case(case, out=out, workspace=ws)  # first call outside capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        k3da.run_case(case, out=out, workspace=ws, stream=s)
+    for seed in [11, 12, 13]:
+        new = maker(device="cuda", seed=seed)
+        case.qkv.copy_(new.qkv)
+        case.ctx_lens.copy_(new.ctx_lens)
+        case.page_table.copy_(new.page_table)
+        case.positions.copy_(new.positions)
+        g.replay()
+        torch.cuda.synchronize()
+        replayed = out.clone()
+        eager = k3da.run_case(case, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(replayed.view(torch.int16), eager.view(torch.int16))
+        assert_close(replayed, oracle_for(case), f"replay seed {seed}")

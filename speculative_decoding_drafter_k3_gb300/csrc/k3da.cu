@@ -53,8 +53,11 @@ constexpr int kRows = 48;        // kG * max block length
 constexpr int kMaxR = 8;
 constexpr int kMaxB = 8;
 constexpr int kMaxUnits = 32;    // 8 requests x 4 kv heads
-constexpr int kConsumerWarps = 3;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kRowWarps = 3;      // 16 query rows each
+constexpr int kKeyGroups = 2;     // each page's 64 keys split in two halves
+constexpr int kConsumerWarps = kRowWarps * kKeyGroups;
+constexpr int kConsumerThreads = 32 * kConsumerWarps;
+constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kTileBytes = kP * kD * 2;       // 8 KB: one page, one head, K or V
 constexpr int kStageBytes = 2 * kTileBytes;   // K + V
 constexpr int kStages = 4;
@@ -68,13 +71,16 @@ constexpr int kOffStages = 0;
 constexpr int kOffQ = kStages * kStageBytes;          // 48 rows x 128 B
 constexpr int kOffBlkK = kOffQ + kRows * 128;         // 16 rows x 128 B
 constexpr int kOffBlkV = kOffBlkK + 16 * 128;
-constexpr int kOffTrig = kOffBlkV + 16 * 128;         // [8][32] float2
-constexpr int kOffUnit = kOffTrig + kMaxB * 32 * 8;   // [33] int64
+constexpr int kOffRaw = kOffBlkV + 16 * 128;          // raw q [8][6][64], k [8][64], v [8][64]
+constexpr int kOffTrig = kOffRaw + kMaxB * (kG + 2) * kD * 2;  // [8][32] float2
+constexpr int kOffMerge = kOffTrig + kMaxB * 32 * 8;  // [3][36][32] float
+constexpr int kOffUnit = kOffMerge + kRowWarps * 36 * 32 * 4;  // [33] int64
 constexpr int kOffLens = kOffUnit + (kMaxUnits + 1) * 8;
-constexpr int kOffBar = kOffLens + kMaxR * 4 + 32;    // 2*kStages mbarriers
+constexpr int kOffBar = kOffLens + kMaxR * 4 + 24;    // 2*kStages mbarriers
 constexpr int kOffFlag = kOffBar + 2 * kStages * 8;
 constexpr int kSmemUsed = kOffFlag + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;          // slack for alignment
+static_assert(kOffBar % 8 == 0 && kOffUnit % 8 == 0, "mbarrier / int64 alignment");
 
 struct Params {
     __nv_bfloat16 *out;
@@ -158,12 +164,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     return mbar_wait_slow(bar, parity, abort_flag, status);
 }
 
-__device__ __forceinline__ void tma_load_tile(uint32_t dst, const CUtensorMap *map, int row,
-                                              uint32_t bar) {
+__device__ __forceinline__ void tma_load_tile(uint32_t dst, const CUtensorMap *map, int row, uint32_t bar,
+                                              uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(bar)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(bar), "l"(policy)
         : "memory");
 }
 
@@ -269,36 +275,37 @@ __device__ __forceinline__ int cta_of_item(long long i, long long W, long long C
 
 struct RowState {
     float m[2];   // running max (log2 units) of rows a = lane/4 and b = a + 8
-    float l[2];   // running sum (this lane's share)
+    float l[2];   // running sum (this lane's share of the row)
     float o[8][4];
 };
 
-// One tile of NKT*16 keys: K rows and V rows at kbase / vbase (swizzled).
-// valid = keys of the tile that are real (the rest are masked out).
-template <int NKT>
+// Attend the warp's 16 query rows to NT*8 keys of a staged tile: K rows and
+// V rows key0 .. key0 + NT*8 - 1 of the tiles at kbase / vbase (128-byte
+// swizzled).  valid (>= 1) = how many of those keys are real; the rest are
+// masked out of the softmax and their values zeroed.
+template <int NT>
 __device__ __forceinline__ void attend_tile(RowState &st, const uint32_t (&qf)[4][4],
-                                            uint32_t kbase, uint32_t vbase, int valid,
+                                            uint32_t kbase, uint32_t vbase, int key0, int valid,
                                             float scale_log2, int lane) {
-    constexpr int NT = 2 * NKT;  // n-tiles of 8 keys
+    static_assert(NT % 2 == 0, "keys come in 16-key steps");
     float s[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-    }
+    for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
     const int mi = lane >> 3, rr = lane & 7;
-    // S = Q K^T: B operand = K rows (keys) with dims contiguous.
+    // S = Q K^T; B operand = K rows (keys) with dims contiguous.
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
         for (int kk2 = 0; kk2 < 2; ++kk2) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(kbase + swz(nt * 8 + rr, kk2 * 4 + mi), b0, b1, b2, b3);
+            ldsm_x4(kbase + swz(key0 + nt * 8 + rr, kk2 * 4 + mi), b0, b1, b2, b3);
             mma_bf16(s[nt], qf[2 * kk2], b0, b1);
             mma_bf16(s[nt], qf[2 * kk2 + 1], b2, b3);
         }
     }
     const int kq = 2 * (lane & 3);
-    if (valid < NKT * 16) {
+    const bool partial = valid < NT * 8;
+    if (partial) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int key = nt * 8 + kq;
@@ -306,7 +313,7 @@ __device__ __forceinline__ void attend_tile(RowState &st, const uint32_t (&qf)[4
             if (key + 1 >= valid) { s[nt][1] = -INFINITY; s[nt][3] = -INFINITY; }
         }
     }
-    // Online softmax, base 2, scale folded into the exponent.
+    // Online softmax in base 2 with the scale folded into the exponent.
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -347,27 +354,29 @@ __device__ __forceinline__ void attend_tile(RowState &st, const uint32_t (&qf)[4
         st.o[nd][2] *= alpha[1];
         st.o[nd][3] *= alpha[1];
     }
-    // O += P V: A operand = P straight from the score registers, B operand =
+    // O += P V: A operand = P straight from the score registers; B operand =
     // V rows (keys) read transposed.
 #pragma unroll
-    for (int kk = 0; kk < NKT; ++kk) {
+    for (int kk = 0; kk < NT / 2; ++kk) {
         const uint32_t a[4] = {pf[2 * kk][0], pf[2 * kk][1], pf[2 * kk + 1][0], pf[2 * kk + 1][1]};
+        uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
+        if (partial) {
+            // Values of masked keys are zeroed so that stale non-finite pool
+            // contents cannot reach the accumulator (0 * inf).
+            const int k0 = kk * 16 + kq;
+            keep_lo = ((k0 < valid) ? 0x0000ffffu : 0u) | ((k0 + 1 < valid) ? 0xffff0000u : 0u);
+            keep_hi = ((k0 + 8 < valid) ? 0x0000ffffu : 0u) | ((k0 + 9 < valid) ? 0xffff0000u : 0u);
+        }
 #pragma unroll
         for (int ndp = 0; ndp < 4; ++ndp) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(vbase + swz(kk * 16 + (mi & 1) * 8 + rr, ndp * 2 + (mi >> 1)), b0, b1, b2, b3);
-            if (valid < NKT * 16) {
-                // Zero the values of masked keys so that stale non-finite
-                // pool contents cannot reach the accumulator (0 * inf).
-                const int k0 = kk * 16 + kq;
-                const uint32_t lo0 = (k0 < valid) ? 0x0000ffffu : 0u;
-                const uint32_t hi0 = (k0 + 1 < valid) ? 0xffff0000u : 0u;
-                const uint32_t lo1 = (k0 + 8 < valid) ? 0x0000ffffu : 0u;
-                const uint32_t hi1 = (k0 + 9 < valid) ? 0xffff0000u : 0u;
-                b0 &= lo0 | hi0;
-                b2 &= lo0 | hi0;
-                b1 &= lo1 | hi1;
-                b3 &= lo1 | hi1;
+            ldsm_x4_t(vbase + swz(key0 + kk * 16 + (mi & 1) * 8 + rr, ndp * 2 + (mi >> 1)), b0, b1, b2,
+                      b3);
+            if (partial) {
+                b0 &= keep_lo;
+                b2 &= keep_lo;
+                b1 &= keep_hi;
+                b3 &= keep_hi;
             }
             mma_bf16(st.o[2 * ndp], a, b0, b1);
             mma_bf16(st.o[2 * ndp + 1], a, b2, b3);
@@ -375,39 +384,55 @@ __device__ __forceinline__ void attend_tile(RowState &st, const uint32_t (&qf)[4
     }
 }
 
-// RMSNorm (optional) + NeoX RoPE (optional) of one 64-wide head row held
-// as x_lo = dim lane, x_hi = dim lane + 32; stores bf16 into a swizzled tile.
+// RMSNorm (QKNORM) and NeoX RoPE (QKNORM) of one 64-wide head row whose
+// dims lane and lane + 32 are x_lo, x_hi; writes the bf16 result into row
+// `row` of a swizzled tile.  w_lo / w_hi are the norm weights of those dims.
 template <bool QKNORM>
-__device__ __forceinline__ void prep_row(uint8_t *tile, int row, float x_lo, float x_hi,
-                                         const __nv_bfloat16 *w, float eps, float2 cs, int lane) {
+__device__ __forceinline__ void prep_row(uint8_t *tile, int row, float x_lo, float x_hi, float w_lo,
+                                         float w_hi, float eps, float2 cs, int lane) {
     float y_lo = x_lo, y_hi = x_hi;
     if (QKNORM) {
         float ss = x_lo * x_lo + x_hi * x_hi;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
         const float inv = rsqrtf(ss * (1.0f / kD) + eps);
-        const float n_lo = x_lo * inv * __bfloat162float(w[lane]);
-        const float n_hi = x_hi * inv * __bfloat162float(w[lane + 32]);
+        const float n_lo = x_lo * inv * w_lo;
+        const float n_hi = x_hi * inv * w_hi;
         y_lo = n_lo * cs.x - n_hi * cs.y;
         y_hi = n_hi * cs.x + n_lo * cs.y;
     }
-    *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, lane >> 3) + (lane & 7) * 2) =
-        __float2bfloat16_rn(y_lo);
+    *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, lane >> 3) + (lane & 7) * 2) = __float2bfloat16_rn(y_lo);
     *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, 4 + (lane >> 3)) + (lane & 7) * 2) =
         __float2bfloat16_rn(y_hi);
 }
 
 __device__ __forceinline__ void zero_row(uint8_t *tile, int row, int lane) {
-    *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, lane >> 3) + (lane & 7) * 2) =
-        __float2bfloat16_rn(0.f);
-    *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, 4 + (lane >> 3)) + (lane & 7) * 2) =
-        __float2bfloat16_rn(0.f);
+    const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
+    *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, lane >> 3) + (lane & 7) * 2) = z;
+    *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, 4 + (lane >> 3)) + (lane & 7) * 2) = z;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ float bf16_at(const uint8_t *base, int index) {
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[index]);
 }
 
 // ------------------------------------------------------------ split pass --
+//
+// Warps 0..5 consume, warp 6 produces.  Consumer warp w works on query rows
+// 16*(w % 3) .. +15 (row = g*B + i for q head 6h + g, token i) and on keys
+// 32*(w / 3) .. +31 of every staged page (key group w / 3); the two key
+// groups keep separate softmax states and merge at the end of each range.
 
 template <bool QKNORM>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __maxnreg__(144)
     k3da_split_kernel(const __grid_constant__ CUtensorMap pool_map, const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -441,6 +466,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------ producer warp --
+        uint64_t policy;
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
         long long k = 0;  // pages issued by this CTA
         long long i = beg;
         for (int u = u0; i < end; ++u) {
@@ -466,9 +493,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                             mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
                             const int krow = ((page * 2 + 0) * p.Hkv + h) * kP;
                             const int vrow = ((page * 2 + 1) * p.Hkv + h) * kP;
-                            tma_load_tile(smem_u32(stage), &pool_map, krow, bar_full + 8 * s);
-                            tma_load_tile(smem_u32(stage + kTileBytes), &pool_map, vrow,
-                                          bar_full + 8 * s);
+                            tma_load_tile(smem_u32(stage), &pool_map, krow, bar_full + 8 * s, policy);
+                            tma_load_tile(smem_u32(stage + kTileBytes), &pool_map, vrow, bar_full + 8 * s,
+                                          policy);
                         }
                     } else {
                         // Out-of-range page id: flag it and serve zeros.
@@ -484,8 +511,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             i = seg_end;
         }
-        // Drain: every issued load must have landed before the CTA exits
-        // (only matters when a wait gave up and the consumers stopped early).
+        // Drain: every issued load must land before the CTA exits (matters
+        // only when a wait gave up and the consumers stopped early).
         if (*abort_flag) {
             for (long long j = (k > kStages ? k - kStages : 0); j < k; ++j) {
                 const int s = static_cast<int>(j % kStages);
@@ -499,15 +526,28 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     // ------------------------------------------------------ consumer warps --
-    const int ctid = threadIdx.x;  // 0..95
+    const int ctid = threadIdx.x;            // 0 .. kConsumerThreads-1
+    const int rb = warp % kRowWarps;         // query row block
+    const int grp = warp / kRowWarps;        // key group
     uint8_t *qtile = smem + kOffQ;
     uint8_t *bk = smem + kOffBlkK;
     uint8_t *bv = smem + kOffBlkV;
+    uint8_t *raw_q = smem + kOffRaw;                  // [B][6][64] bf16
+    uint8_t *raw_k = raw_q + kMaxB * kG * kD * 2;     // [B][64]
+    uint8_t *raw_v = raw_k + kMaxB * kD * 2;          // [B][64]
     float2 *trig = reinterpret_cast<float2 *>(smem + kOffTrig);
+    float *merge = reinterpret_cast<float *>(smem + kOffMerge);
     const int rows = kG * p.B;
-    const bool active = warp * 16 < rows;
+    const bool active = rb * 16 < rows;
     const long long row_w = static_cast<long long>(p.Hq + 2 * p.Hkv) * kD;
     const int mi = lane >> 3, rr = lane & 7;
+    float wq_lo = 1.f, wq_hi = 1.f, wk_lo = 1.f, wk_hi = 1.f;
+    if (QKNORM) {
+        wq_lo = __bfloat162float(p.q_w[lane]);
+        wq_hi = __bfloat162float(p.q_w[lane + 32]);
+        wk_lo = __bfloat162float(p.k_w[lane]);
+        wk_hi = __bfloat162float(p.k_w[lane + 32]);
+    }
     long long k = 0;
     long long i = beg;
     for (int u = u0; i < end; ++u) {
@@ -515,58 +555,85 @@ __global__ void __launch_bounds__(kThreads, 2)
         const long long a = i - ustart[u], b = seg_end - ustart[u];
         const int r = u / p.Hkv, h = u - r * p.Hkv;
         const int L = lens[r];
+        const bool with_block = a == 0;
 
-        named_bar_sync(1, 32 * kConsumerWarps);  // previous range is done with the tiles
+        // ---- stage this unit's q (and block k, v) rows: one round trip.
+        named_bar_sync(1, kConsumerThreads);  // the previous range is done with every tile
+        const char *qkv_rows = reinterpret_cast<const char *>(p.qkv) + static_cast<long long>(r) * p.B * row_w * 2;
+        for (int e = ctid; e < p.B * 48; e += kConsumerThreads) {
+            const int ti = e / 48, c = e - ti * 48;
+            cp_async16(smem_u32(raw_q) + ti * 768 + c * 16,
+                       qkv_rows + ti * row_w * 2 + static_cast<long long>(h) * 768 + c * 16);
+        }
+        if (with_block) {
+            for (int e = ctid; e < p.B * 16; e += kConsumerThreads) {
+                const int ti = e >> 4, c = e & 15;
+                const long long head = c < 8 ? p.Hq + h : p.Hq + p.Hkv + h;
+                cp_async16(smem_u32(c < 8 ? raw_k : raw_v) + ti * 128 + (c & 7) * 16,
+                           qkv_rows + ti * row_w * 2 + head * 128 + (c & 7) * 16);
+            }
+        }
         if (QKNORM) {
-            for (int e = ctid; e < p.B * 32; e += 32 * kConsumerWarps) {
-                const int ti = e >> 5, j = e & 31;
-                const long long t = static_cast<long long>(r) * p.B + ti;
-                const long long pos = p.pos_i64 ? reinterpret_cast<const long long *>(p.positions)[t]
-                                                : reinterpret_cast<const int *>(p.positions)[t];
-                // Angle in fp64, reduced to [-pi, pi] before the fp32 sincos.
-                const double theta = static_cast<double>(pos) * p.inv_freq[j];
-                const double turns = rint(theta * 0.15915494309189535);
-                double red = fma(-turns, 6.283185307179586, theta);
-                red = fma(-turns, 2.4492935982947064e-16, red);
-                float sn, cs;
-                sincosf(static_cast<float>(red), &sn, &cs);
-                trig[ti * 32 + j] = make_float2(cs, sn);
+            // RoPE angles of the B tokens: fp64 product and reduction to
+            // [-pi, pi], then an accurate fp32 sincos.
+            long long pos[2] = {0, 0};
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int e = ctid + q * kConsumerThreads;
+                if (e < p.B * 32) {
+                    const long long t = static_cast<long long>(r) * p.B + (e >> 5);
+                    pos[q] = p.pos_i64 ? reinterpret_cast<const long long *>(p.positions)[t]
+                                       : reinterpret_cast<const int *>(p.positions)[t];
+                }
             }
-            named_bar_sync(1, 32 * kConsumerWarps);
-        }
-        // Query rows: row = g*B + i for q head h*6 + g, token i.
-        for (int row = warp; row < kRows; row += kConsumerWarps) {
-            if (row < rows) {
-                const int g = row / p.B, ti = row - g * p.B;
-                const long long t = static_cast<long long>(r) * p.B + ti;
-                const __nv_bfloat16 *src = p.qkv + t * row_w + static_cast<long long>(h * kG + g) * kD;
-                const float x_lo = __bfloat162float(src[lane]);
-                const float x_hi = __bfloat162float(src[lane + 32]);
-                prep_row<QKNORM>(qtile, row, x_lo, x_hi, p.q_w, p.eps,
-                                 QKNORM ? trig[ti * 32 + lane] : make_float2(1.f, 0.f), lane);
-            } else {
-                zero_row(qtile, row, lane);
-            }
-        }
-        if (a == 0) {
-            // The block's own keys (normalised + roped) and values (raw).
-            for (int j = warp; j < 16; j += kConsumerWarps) {
-                if (j < p.B) {
-                    const long long t = static_cast<long long>(r) * p.B + j;
-                    const __nv_bfloat16 *ks = p.qkv + t * row_w + static_cast<long long>(p.Hq + h) * kD;
-                    const __nv_bfloat16 *vs = p.qkv + t * row_w + static_cast<long long>(p.Hq + p.Hkv + h) * kD;
-                    prep_row<QKNORM>(bk, j, __bfloat162float(ks[lane]), __bfloat162float(ks[lane + 32]),
-                                     p.k_w, p.eps, QKNORM ? trig[j * 32 + lane] : make_float2(1.f, 0.f),
-                                     lane);
-                    prep_row<false>(bv, j, __bfloat162float(vs[lane]), __bfloat162float(vs[lane + 32]),
-                                    nullptr, 0.f, make_float2(1.f, 0.f), lane);
-                } else {
-                    zero_row(bk, j, lane);
-                    zero_row(bv, j, lane);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int e = ctid + q * kConsumerThreads;
+                if (e < p.B * 32) {
+                    const double theta = static_cast<double>(pos[q]) * p.inv_freq[e & 31];
+                    const double turns = rint(theta * 0.15915494309189535);
+                    double red = fma(-turns, 6.283185307179586, theta);
+                    red = fma(-turns, 2.4492935982947064e-16, red);
+                    float sn, cs;
+                    sincosf(static_cast<float>(red), &sn, &cs);
+                    trig[e] = make_float2(cs, sn);
                 }
             }
         }
-        named_bar_sync(1, 32 * kConsumerWarps);
+        cp_async_wait_all();
+        named_bar_sync(1, kConsumerThreads);
+
+        // ---- normalise / rotate into the swizzled operand tiles.
+        const int prep_rows = with_block ? kRows + 32 : kRows;
+        for (int pr = warp; pr < prep_rows; pr += kConsumerWarps) {
+            if (pr < kRows) {
+                if (pr < rows) {
+                    const int g = pr / p.B, ti = pr - g * p.B;
+                    const int idx = (ti * kG + g) * kD;
+                    prep_row<QKNORM>(qtile, pr, bf16_at(raw_q, idx + lane), bf16_at(raw_q, idx + lane + 32),
+                                     wq_lo, wq_hi, p.eps, QKNORM ? trig[ti * 32 + lane] : make_float2(1.f, 0.f),
+                                     lane);
+                } else {
+                    zero_row(qtile, pr, lane);
+                }
+            } else if (pr < kRows + 16) {
+                const int j = pr - kRows;
+                if (j < p.B)
+                    prep_row<QKNORM>(bk, j, bf16_at(raw_k, j * kD + lane), bf16_at(raw_k, j * kD + lane + 32),
+                                     wk_lo, wk_hi, p.eps, QKNORM ? trig[j * 32 + lane] : make_float2(1.f, 0.f),
+                                     lane);
+                else
+                    zero_row(bk, j, lane);
+            } else {
+                const int j = pr - kRows - 16;
+                if (j < p.B)
+                    prep_row<false>(bv, j, bf16_at(raw_v, j * kD + lane), bf16_at(raw_v, j * kD + lane + 32), 1.f,
+                                    1.f, 0.f, make_float2(1.f, 0.f), lane);
+                else
+                    zero_row(bv, j, lane);
+            }
+        }
+        named_bar_sync(1, kConsumerThreads);
 
         RowState st;
         st.m[0] = st.m[1] = -INFINITY;
@@ -575,106 +642,172 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int nd = 0; nd < 8; ++nd) st.o[nd][0] = st.o[nd][1] = st.o[nd][2] = st.o[nd][3] = 0.f;
         uint32_t qf[4][4];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            ldsm_x4(smem_u32(qtile) + swz(warp * 16 + (mi & 1) * 8 + rr, kk * 2 + (mi >> 1)),
-                    qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-        }
+        for (int kk = 0; kk < 4; ++kk)
+            ldsm_x4(smem_u32(qtile) + swz(rb * 16 + (mi & 1) * 8 + rr, kk * 2 + (mi >> 1)), qf[kk][0], qf[kk][1],
+                    qf[kk][2], qf[kk][3]);
 
-        if (a == 0 && active) {
-            attend_tile<1>(st, qf, smem_u32(bk), smem_u32(bv), p.B, p.scale_log2, lane);
-        }
+        if (with_block && grp == 0 && active)
+            attend_tile<2>(st, qf, smem_u32(bk), smem_u32(bv), 0, p.B, p.scale_log2, lane);
         const long long pa = a == 0 ? 0 : a - 1, pb = b - 1;
         for (long long pg = pa; pg < pb; ++pg, ++k) {
             const int s = static_cast<int>(k % kStages);
             const uint32_t par = static_cast<uint32_t>((k / kStages) & 1);
             const bool ok = mbar_wait(bar_full + 8 * s, par, abort_flag, p.status);
-            if (active && ok) {
-                const long long left = static_cast<long long>(L) - pg * kP;
-                const int valid = left < kP ? static_cast<int>(left) : kP;
+            const long long left = static_cast<long long>(L) - pg * kP - grp * 32;
+            if (active && ok && left > 0) {
+                const int valid = left < 32 ? static_cast<int>(left) : 32;
                 const uint32_t stage = smem_u32(smem + kOffStages + s * kStageBytes);
-                attend_tile<4>(st, qf, stage, stage + kTileBytes, valid, p.scale_log2, lane);
+                attend_tile<4>(st, qf, stage, stage + kTileBytes, grp * 32, valid, p.scale_log2, lane);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * s);
         }
 
-        // Partial of this (CTA, unit) range.
-        if (active) {
+        // ---- merge the two key groups, write this (CTA, unit) partial.
+        float *mine = merge + (rb * 36) * 32 + lane;  // [row block][36 values][lane]
+        if (grp == 1 && active) {
+#pragma unroll
+            for (int nd = 0; nd < 8; ++nd)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) mine[(nd * 4 + c) * 32] = st.o[nd][c];
+            mine[32 * 32] = st.m[0];
+            mine[33 * 32] = st.m[1];
+            mine[34 * 32] = st.l[0];
+            mine[35 * 32] = st.l[1];
+        }
+        named_bar_sync(1, kConsumerThreads);
+        if (grp == 0 && active) {
+            float f0[2], f1[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float m1 = mine[(32 + e) * 32];
+                const float mm = fmaxf(st.m[e], m1);
+                f0[e] = exp2_approx(st.m[e] - mm);
+                f1[e] = exp2_approx(m1 - mm);  // 0 when the other group saw no key
+                st.m[e] = mm;
+                st.l[e] = st.l[e] * f0[e] + mine[(34 + e) * 32] * f1[e];
+            }
+#pragma unroll
+            for (int nd = 0; nd < 8; ++nd) {
+                st.o[nd][0] = st.o[nd][0] * f0[0] + mine[(nd * 4 + 0) * 32] * f1[0];
+                st.o[nd][1] = st.o[nd][1] * f0[0] + mine[(nd * 4 + 1) * 32] * f1[0];
+                st.o[nd][2] = st.o[nd][2] * f0[1] + mine[(nd * 4 + 2) * 32] * f1[1];
+                st.o[nd][3] = st.o[nd][3] * f0[1] + mine[(nd * 4 + 3) * 32] * f1[1];
+            }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 st.l[e] += __shfl_xor_sync(kFull, st.l[e], 1);
                 st.l[e] += __shfl_xor_sync(kFull, st.l[e], 2);
             }
             const long long slot = static_cast<long long>(blockIdx.x) + u;
-            const int ra = warp * 16 + (lane >> 2), rb = ra + 8;
+            const int ra = rb * 16 + (lane >> 2), rbw = ra + 8;
             float *ob = p.ws_o + slot * kPartialFloats;
             const int dq = 2 * (lane & 3);
 #pragma unroll
             for (int nd = 0; nd < 8; ++nd) {
                 if (ra < rows)
                     *reinterpret_cast<float2 *>(ob + ra * kD + nd * 8 + dq) = make_float2(st.o[nd][0], st.o[nd][1]);
-                if (rb < rows)
-                    *reinterpret_cast<float2 *>(ob + rb * kD + nd * 8 + dq) = make_float2(st.o[nd][2], st.o[nd][3]);
+                if (rbw < rows)
+                    *reinterpret_cast<float2 *>(ob + rbw * kD + nd * 8 + dq) = make_float2(st.o[nd][2], st.o[nd][3]);
             }
             if ((lane & 3) == 0) {
                 if (ra < rows) p.ws_ml[slot * kRows + ra] = make_float2(st.m[0], st.l[0]);
-                if (rb < rows) p.ws_ml[slot * kRows + rb] = make_float2(st.m[1], st.l[1]);
+                if (rbw < rows) p.ws_ml[slot * kRows + rbw] = make_float2(st.m[1], st.l[1]);
             }
         }
         i = seg_end;
     }
+    // Let the combine grid start launching; it waits for this grid to finish.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // --------------------------------------------------------------- combine --
 //
-// One CTA per (unit, 16-row chunk); thread = (row, 8 dims).  Merges the
-// unit's partials in CTA order and writes the bf16 output row slice.
-__global__ void __launch_bounds__(128) k3da_combine_kernel(const __grid_constant__ Params p) {
+// One CTA per (unit, 4 query rows), 256 threads: thread = (row, segment
+// lane sg of 8, 8 dims).  Each thread merges the unit's partials sg, sg+8,
+// ... online; the 8 segment lanes then merge in fixed order through shared
+// memory, so the result does not depend on timing.  Launched as a
+// programmatic dependent of the split pass: the prologue overlaps its tail
+// and griddepcontrol.wait orders the partial reads after it.
+__global__ void __launch_bounds__(256) k3da_combine_kernel(const __grid_constant__ Params p) {
     __shared__ long long ustart[kMaxUnits + 1];
     __shared__ int lens[kMaxR];
+    __shared__ float red[4][8][10];
     build_partition(p, lens, ustart, false);
     __syncthreads();
-    const int u = blockIdx.x / 3, chunk = blockIdx.x - 3 * (blockIdx.x / 3);
-    const int row = chunk * 16 + (threadIdx.x >> 3);
+    const int u = blockIdx.x / (kRows / 4);
+    const int row = (blockIdx.x - u * (kRows / 4)) * 4 + (threadIdx.x >> 6);
+    const int sg = (threadIdx.x >> 3) & 7, dc = threadIdx.x & 7;
     const int rows = kG * p.B;
-    if (row >= rows) return;
-    const int d0 = (threadIdx.x & 7) * 8;
     const int U = p.R * p.Hkv;
     const long long W = ustart[U];
     const long long C = W < p.grid ? W : p.grid;
     const int c0 = cta_of_item(ustart[u], W, C);
     const int c1 = cta_of_item(ustart[u + 1] - 1, W, C);
-    float M = -INFINITY;
-    for (int c = c0; c <= c1; ++c) M = fmaxf(M, p.ws_ml[(static_cast<long long>(c) + u) * kRows + row].x);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    float m = -INFINITY, l = 0.f;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float lsum = 0.f;
-    for (int c = c0; c <= c1; ++c) {
-        const long long slot = static_cast<long long>(c) + u;
-        const float2 ml = p.ws_ml[slot * kRows + row];
-        const float w = exp2_approx(ml.x - M);
-        lsum = fmaf(ml.y, w, lsum);
-        const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + slot * kPartialFloats + row * kD + d0);
-        const float4 v0 = src[0], v1 = src[1];
-        acc[0] = fmaf(v0.x, w, acc[0]);
-        acc[1] = fmaf(v0.y, w, acc[1]);
-        acc[2] = fmaf(v0.z, w, acc[2]);
-        acc[3] = fmaf(v0.w, w, acc[3]);
-        acc[4] = fmaf(v1.x, w, acc[4]);
-        acc[5] = fmaf(v1.y, w, acc[5]);
-        acc[6] = fmaf(v1.z, w, acc[6]);
-        acc[7] = fmaf(v1.w, w, acc[7]);
+    if (row < rows) {
+        for (int c = c0 + sg; c <= c1; c += 8) {
+            const long long slot = static_cast<long long>(c) + u;
+            const float2 ml = p.ws_ml[slot * kRows + row];
+            const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + slot * kPartialFloats + row * kD + dc * 8);
+            const float4 v0 = src[0], v1 = src[1];
+            const float mm = fmaxf(m, ml.x);
+            const float fo = exp2_approx(m - mm), fn = exp2_approx(ml.x - mm);
+            m = mm;
+            l = l * fo + ml.y * fn;
+            acc[0] = acc[0] * fo + v0.x * fn;
+            acc[1] = acc[1] * fo + v0.y * fn;
+            acc[2] = acc[2] * fo + v0.z * fn;
+            acc[3] = acc[3] * fo + v0.w * fn;
+            acc[4] = acc[4] * fo + v1.x * fn;
+            acc[5] = acc[5] * fo + v1.y * fn;
+            acc[6] = acc[6] * fo + v1.z * fn;
+            acc[7] = acc[7] * fo + v1.w * fn;
+        }
     }
-    const float inv = 1.0f / lsum;
-    const int r = u / p.Hkv, h = u - r * p.Hkv;
-    const int g = row / p.B, ti = row - g * p.B;
-    const long long t = static_cast<long long>(r) * p.B + ti;
-    uint4 packed;
-    packed.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-    packed.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-    packed.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-    packed.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-    *reinterpret_cast<uint4 *>(p.out + t * (static_cast<long long>(p.Hq) * kD) +
-                               static_cast<long long>(h * kG + g) * kD + d0) = packed;
+    // Fixed-order merge of the 8 segment lanes, one dim chunk at a time.
+    const int rl = threadIdx.x >> 6;
+    float outv[8];
+    for (int d = 0; d < 8; ++d) {
+        __syncthreads();
+        if (dc == d) {
+            red[rl][sg][0] = m;
+            red[rl][sg][1] = l;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) red[rl][sg][2 + j] = acc[j];
+        }
+        __syncthreads();
+        if (dc == d && sg == 0) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) M = fmaxf(M, red[rl][q][0]);
+            float lt = 0.f, at[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float f = exp2_approx(red[rl][q][0] - M);  // 0 for empty lanes
+                lt = fmaf(red[rl][q][1], f, lt);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) at[j] = fmaf(red[rl][q][2 + j], f, at[j]);
+            }
+            const float inv = 1.0f / lt;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) outv[j] = at[j] * inv;
+        }
+    }
+    if (sg == 0 && row < rows) {
+        const int r = u / p.Hkv, h = u - r * p.Hkv;
+        const int g = row / p.B, ti = row - g * p.B;
+        const long long t = static_cast<long long>(r) * p.B + ti;
+        uint4 packed;
+        packed.x = pack_bf16(outv[0], outv[1]);
+        packed.y = pack_bf16(outv[2], outv[3]);
+        packed.z = pack_bf16(outv[4], outv[5]);
+        packed.w = pack_bf16(outv[6], outv[7]);
+        *reinterpret_cast<uint4 *>(p.out + t * (static_cast<long long>(p.Hq) * kD) +
+                                   static_cast<long long>(h * kG + g) * kD + dc * 8) = packed;
+    }
 }
 
 // ------------------------------------------------------------------ host --
@@ -822,7 +955,20 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
         k3da_split_kernel<false><<<prm.grid, kThreads, kSmemBytes, st>>>(map, prm);
     if (cudaGetLastError() != cudaSuccess) return K3DA_ECUDA;
     if (g_phase_event && cudaEventRecord(g_phase_event, st) != cudaSuccess) return K3DA_ECUDA;
-    k3da_combine_kernel<<<R * Hkv * 3, 128, 0, st>>>(prm);
+    // The combine is a programmatic dependent of the split pass, so its
+    // launch and prologue overlap the split pass's tail.
+    cudaLaunchConfig_t lc;
+    memset(&lc, 0, sizeof lc);
+    lc.gridDim = dim3(static_cast<unsigned>(R * Hkv * (kRows / 4)));
+    lc.blockDim = dim3(256);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&lc, k3da_combine_kernel, prm) != cudaSuccess) return K3DA_ECUDA;
     if (cudaGetLastError() != cudaSuccess) return K3DA_ECUDA;
     return K3DA_OK;
 }

@@ -183,14 +183,21 @@ def split_sweep(R: int, B: int, device="cpu", seed: int = 3) -> Case:
                       num_pages=4096, qknorm=True, pos_dtype=torch.int32, seed=seed, device=device)
 
 
-def long_context(device="cpu", seed: int = 4, num_pages: int = 20000, R: int = 8, B: int = 8) -> Case:
+def long_context(device="cpu", seed: int = 4, num_pages: int = 20000, R: int = 8, B: int = 8,
+                 lo: int = 16384, hi: int = 131072, page_stride: int = 2048) -> Case:
     """8x8, 24/4, fused, int64 positions, lengths U{16384..131072}, a
     20000-page pool, rows of a random page permutation (stride 2048)."""
     g = _gen(seed + 307, "cpu")
-    lens = torch.randint(16384, 131073, (R,), generator=g).tolist()
-    return build_case("long_8x8_24/4_L16k-128k", R=R, B=B, Hq=24, Hkv=4, lens=lens,
-                      page_stride=2048, num_pages=num_pages, qknorm=True, pos_dtype=torch.int64,
-                      seed=seed, device=device)
+    lens = torch.randint(lo, hi + 1, (R,), generator=g).tolist()
+    return build_case(f"long_{R}x{B}_24/4_L{lo // 1024}k-{hi // 1024}k_pool{num_pages}", R=R, B=B,
+                      Hq=24, Hkv=4, lens=lens, page_stride=page_stride, num_pages=num_pages, qknorm=True,
+                      pos_dtype=torch.int64, seed=seed, device=device)
+
+
+def long_context_small(device="cpu", seed: int = 4) -> Case:
+    """The long-context shape at a size meant for profiler captures: lengths
+    U{16384..24576} (~160 MB of K/V read, more than L2), a 4096-page pool."""
+    return long_context(device=device, seed=seed, num_pages=4096, lo=16384, hi=24576, page_stride=384)
 
 
 WORKLOADS = {
@@ -198,4 +205,5 @@ WORKLOADS = {
     "mixed_8x8": mixed_8x8,
     "heads_24_4": heads_24_4,
     "long_context": long_context,
+    "long_context_small": long_context_small,
 }

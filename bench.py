@@ -285,7 +285,7 @@ def run_ours(args, world, rank):
     dev = torch.device("cuda", torch.cuda.current_device())
     case = workloads.WORKLOADS[args.workload](device=dev)
     out = torch.empty(case.T, case.Hq * case.D, dtype=torch.bfloat16, device=dev)
-    ws = k3da.alloc_workspace(case.R, case.B, case.Hq, case.Hkv, dev)
+    ws = k3da.case_workspace(case)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)

@@ -63,13 +63,12 @@ enum {
 typedef enum { K3DA_POS_I32 = 0, K3DA_POS_I64 = 1 } k3da_pos_dtype;
 
 /*
- * Bytes of device workspace a call with these sizes needs on `device`
- * (-1 = the current device).  Returns 0 when the sizes are out of contract
- * or the device cannot be queried.  The value depends on the device's SM
- * count, not on lengths, so one buffer serves every call of a graph.
+ * Bytes of device workspace a call with these sizes needs.  Returns 0 when
+ * the sizes are out of contract.  The value does not depend on lengths or on
+ * the device, so one buffer serves every call of a captured graph.
  */
 size_t k3da_workspace_bytes(int num_requests, int block_len, int num_q_heads,
-                            int num_kv_heads, int device);
+                            int num_kv_heads, int page_stride);
 
 /*
  * k3da_attn -- block attention on already normalised and roped q / k

@@ -87,11 +87,11 @@ def _check(rc: int, what: str):
 
 
 def workspace_bytes(num_requests: int, block_len: int, num_q_heads: int, num_kv_heads: int,
-                    device: int = -1) -> int:
+                    page_stride: int) -> int:
     n = load_library().k3da_workspace_bytes(num_requests, block_len, num_q_heads, num_kv_heads,
-                                            device)
+                                            page_stride)
     if n == 0:
-        raise K3daError("workspace_bytes: sizes out of contract or device not queryable")
+        raise K3daError("workspace_bytes: sizes out of contract")
     return int(n)
 
 
@@ -169,12 +169,15 @@ def k3da_attn_qknorm(out, qkv, kv_pool, page_table, ctx_lens, positions, q_norm_
 
 
 def alloc_workspace(num_requests: int, block_len: int, num_q_heads: int, num_kv_heads: int,
-                    device=None) -> torch.Tensor:
-    """A workspace tensor (uint8, 16-byte aligned) sized for these shapes."""
+                    page_stride: int, device=None) -> torch.Tensor:
+    """A workspace tensor (uint8, 256-byte aligned by torch) for these sizes."""
     device = torch.device("cuda") if device is None else torch.device(device)
-    idx = device.index if device.index is not None else torch.cuda.current_device()
-    n = workspace_bytes(num_requests, block_len, num_q_heads, num_kv_heads, idx)
+    n = workspace_bytes(num_requests, block_len, num_q_heads, num_kv_heads, page_stride)
     return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def case_workspace(case) -> torch.Tensor:
+    return alloc_workspace(case.R, case.B, case.Hq, case.Hkv, case.page_stride, case.qkv.device)
 
 
 def run_case(case, out=None, workspace=None, status=None, stream=None):
@@ -182,7 +185,7 @@ def run_case(case, out=None, workspace=None, status=None, stream=None):
     if out is None:
         out = torch.empty(case.T, case.Hq * case.D, dtype=torch.bfloat16, device=case.qkv.device)
     if workspace is None:
-        workspace = alloc_workspace(case.R, case.B, case.Hq, case.Hkv, case.qkv.device)
+        workspace = case_workspace(case)
     kw = dict(block_len=case.B, num_q_heads=case.Hq, num_kv_heads=case.Hkv,
               softmax_scale=case.scale, workspace=workspace, status=status, stream=stream)
     if case.qknorm:

@@ -12,25 +12,31 @@
 //
 // Design (one GPU, HBM-bound):
 //   * Work unit = (request r, kv head h).  Its items are the block (item 0,
-//     the B block keys) and its context pages (items 1..ceil(L/64)).  All
-//     units' items are laid end to end and cut into equal contiguous ranges,
-//     one per CTA of a grid sized to fill every SM ("stream-K" split), so
-//     uneven context lengths never idle an SM.  The split is computed on the
-//     device from ctx_lens, so a captured graph replays with new lengths.
-//   * A CTA = 3 consumer warps (16 query rows each: 6 q heads x B tokens =
-//     48 rows share one kv head) + 1 producer warp.  The producer walks the
+//     the B block keys) and its context pages (items 1..ceil(L/64)).  A unit
+//     is cut into chunks of ch(u) items, ch(u) = clamp(ceil(items/16), 1,
+//     kChunkMax), so chunk boundaries depend on that unit's length alone.
+//     All units' items are laid end to end; CTA c of the grid (sized to fill
+//     every SM) takes the chunks whose first item falls in the c-th equal
+//     slice of that line.  Long and short contexts thus spread over all SMs,
+//     and every chunk's partial result is the same whatever the other
+//     requests hold: requests are isolated bit for bit.  The plan is built on
+//     the device from ctx_lens, so a captured graph replays with new lengths.
+//   * A CTA = 6 consumer warps + 1 producer warp.  Consumer warp w owns query
+//     rows 16*(w%3)..+15 (the 6 q heads x B tokens = 48 rows that share one
+//     kv head) and keys 32*(w/3)..+31 of every page.  The producer walks the
 //     page table (32 ids per coalesced load, prefetched a batch ahead) and
 //     TMA-loads each page's K tile and V tile (64 x 64 bf16, 8 KB each,
 //     contiguous in the HND pool) into a ring of shared-memory stages with
 //     the 128-byte swizzle, so the ldmatrix reads below are conflict-free.
 //   * Consumers: S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 in,
 //     fp32 accumulate), online softmax in base 2 with the scale folded in.
-//     Q (and, for the unit's first range, the block K/V) are built in shared
-//     memory at the start of each range: RMSNorm and RoPE happen on the way
-//     in, RoPE angles are reduced in fp64 then turned by an accurate sincosf.
-//   * Each (CTA, unit) range writes an unnormalised partial (O, m, l) to the
-//     workspace; the combine kernel merges a unit's partials in CTA order
-//     (fixed, so reruns are bit-identical) and writes bf16 out.
+//     When a CTA starts on a unit, its q (and block k, v) rows are staged
+//     with one batch of cp.async copies and turned into operand tiles:
+//     RMSNorm and RoPE happen on the way in, RoPE angles are reduced in fp64
+//     then turned by an accurate sincosf.
+//   * Each chunk leaves an unnormalised partial (O, m, l) in the workspace;
+//     the combine kernel folds a unit's chunk partials in a fixed order and
+//     writes bf16 out, so reruns are bit-identical.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -60,8 +66,16 @@ constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kTileBytes = kP * kD * 2;       // 8 KB: one page, one head, K or V
 constexpr int kStageBytes = 2 * kTileBytes;   // K + V
-constexpr int kStages = 4;
-constexpr int kMaxCtasPerSm = 4;
+#ifndef K3DA_STAGES
+#define K3DA_STAGES 4
+#endif
+constexpr int kStages = K3DA_STAGES;
+constexpr int kMaxCtasPerSm = 2;
+constexpr int kChunkSplits = 16;   // a unit is cut into at most this many chunks ...
+#ifndef K3DA_CHUNK_MAX
+#define K3DA_CHUNK_MAX 32
+#endif
+constexpr int kChunkMax = K3DA_CHUNK_MAX;  // ... of at most this many items, beyond which it gets more chunks
 constexpr int kPartialFloats = kRows * kD;    // O of one (CTA, unit) range
 constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
@@ -74,13 +88,12 @@ constexpr int kOffBlkV = kOffBlkK + 16 * 128;
 constexpr int kOffRaw = kOffBlkV + 16 * 128;          // raw q [8][6][64], k [8][64], v [8][64]
 constexpr int kOffTrig = kOffRaw + kMaxB * (kG + 2) * kD * 2;  // [8][32] float2
 constexpr int kOffMerge = kOffTrig + kMaxB * 32 * 8;  // [3][36][32] float
-constexpr int kOffUnit = kOffMerge + kRowWarps * 36 * 32 * 4;  // [33] int64
-constexpr int kOffLens = kOffUnit + (kMaxUnits + 1) * 8;
-constexpr int kOffBar = kOffLens + kMaxR * 4 + 24;    // 2*kStages mbarriers
+constexpr int kOffPlan = kOffMerge + kRowWarps * 36 * 32 * 4;  // struct Plan
+constexpr int kOffBar = kOffPlan + 1536;              // 2*kStages mbarriers
 constexpr int kOffFlag = kOffBar + 2 * kStages * 8;
 constexpr int kSmemUsed = kOffFlag + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;          // slack for alignment
-static_assert(kOffBar % 8 == 0 && kOffUnit % 8 == 0, "mbarrier / int64 alignment");
+static_assert(kOffBar % 8 == 0 && kOffPlan % 8 == 0, "mbarrier / int64 alignment");
 
 struct Params {
     __nv_bfloat16 *out;
@@ -218,57 +231,117 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-// --------------------------------------------------------- work partition --
+// ------------------------------------------------------------ work plan --
 //
-// Items of unit u = r*Hkv + h: 1 (the block) + ceil(L_r/64) (pages).  Units
-// are laid end to end; ustart[u] is the first item of unit u, ustart[U] = W.
-// CTA c of C = min(grid, W) owns items [c*W/C, (c+1)*W/C).
+// Items of unit u = r*Hkv + h: 1 (the block) + ceil(L_r/64) (pages); unit u
+// covers items [ustart[u], ustart[u+1]) of the line, W = ustart[U].  Chunk j
+// of unit u covers its items [j*ch, min((j+1)*ch, items)) and leaves its
+// partial in workspace slot cstart[u] + j.  CTA c of C takes the chunks whose
+// first item lies in [ceil(c*W/C), ceil((c+1)*W/C)): one run of consecutive
+// chunks per unit it touches.
 
-struct Partition {
-    long long W;
-    int C;
+struct Plan {
+    long long ustart[kMaxUnits + 1];
+    int ch[kMaxUnits];
+    int nch[kMaxUnits];
+    int cstart[kMaxUnits + 1];
+    int lens[kMaxR];
+    int nrun;
+    int run_u[kMaxUnits];
+    int run_j0[kMaxUnits];
+    int run_j1[kMaxUnits];
+    int run_p0[kMaxUnits];          // first page of the run
+    int run_pq[kMaxUnits + 1];      // pages of earlier runs (producer sequence)
 };
+static_assert(sizeof(Plan) <= 1536, "plan fits its shared-memory slot");
 
-// Reads and checks ctx_lens with warp 0; fills lens_s[R] and ustart_s[U+1].
-__device__ void build_partition(const Params &p, int *lens_s, long long *ustart_s,
-                                bool report) {
-    const int lane = threadIdx.x & 31;
-    if (threadIdx.x < 32) {
-        int L = 0;
-        if (lane < p.R) {
-            L = __ldg(p.ctx_lens + lane);
-            const int cap = p.page_stride * kP;
-            bool bad = false;
-            if (L < 0) { L = 0; bad = true; }
-            if (L > cap) { L = cap; bad = true; }
-            if (bad && report && p.status) atomicOr(p.status, K3DA_STATUS_BAD_LENGTH);
-            lens_s[lane] = L;
-        }
-        __syncwarp();
-        if (lane == 0) {
-            long long acc = 0;
-            for (int r = 0; r < p.R; ++r) {
-                const long long items = 1 + (lens_s[r] + kP - 1) / kP;
-                for (int h = 0; h < p.Hkv; ++h) {
-                    ustart_s[r * p.Hkv + h] = acc;
-                    acc += items;
-                }
-            }
-            ustart_s[p.R * p.Hkv] = acc;
+__device__ __forceinline__ long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
+
+// Warp 0 reads and checks ctx_lens and builds the plan, one lane per unit
+// with shuffle scans; cta < 0 builds only the unit tables (for the
+// combine).  The caller syncs.
+__device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool report) {
+    if (threadIdx.x >= 32) return;
+    const int lane = threadIdx.x;
+    int L = 0;
+    if (lane < p.R) {
+        L = __ldg(p.ctx_lens + lane);
+        const int cap = p.page_stride * kP;
+        bool bad = false;
+        if (L < 0) { L = 0; bad = true; }
+        if (L > cap) { L = cap; bad = true; }
+        if (bad && report && p.status) atomicOr(p.status, K3DA_STATUS_BAD_LENGTH);
+        pl->lens[lane] = L;
+    }
+    const int U = p.R * p.Hkv;
+    const int u = lane;
+    const int Lu = __shfl_sync(kFull, L, (u < U ? u / p.Hkv : 0));
+    int items = 0, ch = 1, nch = 0;
+    if (u < U) {
+        items = 1 + (Lu + kP - 1) / kP;
+        ch = (items + kChunkSplits - 1) / kChunkSplits;
+        ch = ch < 1 ? 1 : (ch > kChunkMax ? kChunkMax : ch);
+        nch = (items + ch - 1) / ch;
+    }
+    long long si = items;  // inclusive scans over units
+    int sn = nch;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long ti = __shfl_up_sync(kFull, si, off);
+        const int tn = __shfl_up_sync(kFull, sn, off);
+        if (lane >= off) { si += ti; sn += tn; }
+    }
+    const long long base = si - items;
+    if (u < U) {
+        pl->ustart[u] = base;
+        pl->ch[u] = ch;
+        pl->nch[u] = nch;
+        pl->cstart[u] = sn - nch;
+    }
+    const long long W = __shfl_sync(kFull, si, U - 1);
+    const int NC = __shfl_sync(kFull, sn, U - 1);
+    if (lane == 0) {
+        pl->ustart[U] = W;
+        pl->cstart[U] = NC;
+        pl->run_pq[0] = 0;
+        pl->nrun = 0;
+    }
+    if (cta < 0) return;
+    const long long lo = ceil_div_ll(static_cast<long long>(cta) * W, C);
+    const long long hi = ceil_div_ll(static_cast<long long>(cta + 1) * W, C);
+    bool has = false;
+    int j0 = 0, j1 = 0, p0 = 0, npg = 0;
+    if (u < U) {
+        long long a = lo - base <= 0 ? 0 : ceil_div_ll(lo - base, ch);
+        long long b = hi - base <= 0 ? 0 : ceil_div_ll(hi - base, ch);
+        a = a > nch ? nch : a;
+        b = b > nch ? nch : b;
+        if (a < b) {
+            has = true;
+            j0 = static_cast<int>(a);
+            j1 = static_cast<int>(b);
+            const int i0 = j0 * ch;
+            const int i1 = j1 * ch < items ? j1 * ch : items;
+            p0 = i0 == 0 ? 0 : i0 - 1;
+            npg = (i1 - 1) - p0;
         }
     }
-}
-
-__device__ __forceinline__ long long range_begin(long long c, long long W, long long C) {
-    return c * W / C;
-}
-
-// The CTA whose range holds item i.
-__device__ __forceinline__ int cta_of_item(long long i, long long W, long long C) {
-    long long c = i * C / W;
-    while (c + 1 < C && range_begin(c + 1, W, C) <= i) ++c;
-    while (c > 0 && range_begin(c, W, C) > i) --c;
-    return static_cast<int>(c);
+    const unsigned mask = __ballot_sync(kFull, has);
+    int sp = npg;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(kFull, sp, off);
+        if (lane >= off) sp += t;
+    }
+    if (has) {
+        const int idx = __popc(mask & ((1u << lane) - 1u));
+        pl->run_u[idx] = u;
+        pl->run_j0[idx] = j0;
+        pl->run_j1[idx] = j1;
+        pl->run_p0[idx] = p0;
+        pl->run_pq[idx + 1] = sp;
+    }
+    if (lane == 0) pl->nrun = __popc(mask);
 }
 
 // ------------------------------------------------------------- consumers --
@@ -429,22 +502,21 @@ __device__ __forceinline__ float bf16_at(const uint8_t *base, int index) {
 // Warps 0..5 consume, warp 6 produces.  Consumer warp w works on query rows
 // 16*(w % 3) .. +15 (row = g*B + i for q head 6h + g, token i) and on keys
 // 32*(w / 3) .. +31 of every staged page (key group w / 3); the two key
-// groups keep separate softmax states and merge at the end of each range.
+// groups keep separate softmax states and merge at the end of each chunk.
 
 template <bool QKNORM>
-__global__ void __maxnreg__(144)
+__global__ void __launch_bounds__(kThreads, 2)
     k3da_split_kernel(const __grid_constant__ CUtensorMap pool_map, const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    long long *ustart = reinterpret_cast<long long *>(smem + kOffUnit);
-    int *lens = reinterpret_cast<int *>(smem + kOffLens);
+    Plan *pl = reinterpret_cast<Plan *>(smem + kOffPlan);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffFlag);
     const uint32_t bar_full = smem_u32(smem + kOffBar);
     const uint32_t bar_empty = bar_full + kStages * 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    build_partition(p, lens, ustart, blockIdx.x == 0);
+    build_plan(p, pl, blockIdx.x, p.grid, blockIdx.x == 0);
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         for (int s = 0; s < kStages; ++s) {
@@ -454,67 +526,66 @@ __global__ void __maxnreg__(144)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-
-    const int U = p.R * p.Hkv;
-    const long long W = ustart[U];
-    const long long C = W < p.grid ? W : p.grid;
-    if (blockIdx.x >= C) return;
-    const long long beg = range_begin(blockIdx.x, W, C);
-    const long long end = range_begin(blockIdx.x + 1, W, C);
-    int u0 = 0;
-    while (ustart[u0 + 1] <= beg) ++u0;
+    const int nrun = pl->nrun;
+    if (nrun == 0) {
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        return;
+    }
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------ producer warp --
+        // The CTA's pages, run after run, form one sequence; lane l resolves
+        // entry base + l of each 32-entry batch (page id -> TMA row of its K
+        // tile, -1 if out of range), one batch ahead of the loads it feeds.
         uint64_t policy;
         asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
-        long long k = 0;  // pages issued by this CTA
-        long long i = beg;
-        for (int u = u0; i < end; ++u) {
-            const long long seg_end = end < ustart[u + 1] ? end : ustart[u + 1];
-            const long long a = i - ustart[u], b = seg_end - ustart[u];
+        const int total = pl->run_pq[nrun];
+        auto resolve = [&](int q) -> int {
+            if (q >= total) return -1;
+            int k = 0;
+            while (pl->run_pq[k + 1] <= q) ++k;
+            const int u = pl->run_u[k];
             const int r = u / p.Hkv, h = u - r * p.Hkv;
-            const long long pa = a == 0 ? 0 : a - 1, pb = b - 1;
-            const int n = static_cast<int>(pb - pa);
-            const int32_t *row = p.page_table + static_cast<long long>(r) * p.page_stride + pa;
-            int next = lane < n ? __ldg(row + lane) : 0;
-            for (int base = 0; base < n; base += 32) {
-                const int ids = next;
-                if (base + 32 < n) next = (base + 32 + lane < n) ? __ldg(row + base + 32 + lane) : 0;
-                const int cnt = n - base < 32 ? n - base : 32;
-                for (int j = 0; j < cnt; ++j, ++k) {
-                    const int page = __shfl_sync(kFull, ids, j);
-                    const int s = static_cast<int>(k % kStages);
-                    const uint32_t par = static_cast<uint32_t>((k / kStages) & 1);
-                    mbar_wait(bar_empty + 8 * s, par ^ 1u, abort_flag, p.status);
-                    uint8_t *stage = smem + kOffStages + s * kStageBytes;
-                    if (page >= 0 && page < p.num_pages) {
-                        if (lane == 0) {
-                            mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
-                            const int krow = ((page * 2 + 0) * p.Hkv + h) * kP;
-                            const int vrow = ((page * 2 + 1) * p.Hkv + h) * kP;
-                            tma_load_tile(smem_u32(stage), &pool_map, krow, bar_full + 8 * s, policy);
-                            tma_load_tile(smem_u32(stage + kTileBytes), &pool_map, vrow, bar_full + 8 * s,
-                                          policy);
-                        }
-                    } else {
-                        // Out-of-range page id: flag it and serve zeros.
-                        if (lane == 0 && p.status) atomicOr(p.status, K3DA_STATUS_BAD_PAGE);
-                        uint4 *dst = reinterpret_cast<uint4 *>(stage);
-                        for (int q = lane; q < kStageBytes / 16; q += 32) dst[q] = make_uint4(0, 0, 0, 0);
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar_full + 8 * s);
+            const int page = __ldg(p.page_table + static_cast<long long>(r) * p.page_stride + pl->run_p0[k] +
+                                   (q - pl->run_pq[k]));
+            if (page < 0 || page >= p.num_pages) return -1;  // served as zeros, flagged
+            return ((page * 2 + 0) * p.Hkv + h) * kP;
+        };
+        int next = resolve(lane);
+        for (int base = 0; base < total; base += 32) {
+            const int rows_k = next;
+            next = resolve(base + 32 + lane);
+            const int cnt = total - base < 32 ? total - base : 32;
+            for (int j = 0; j < cnt; ++j) {
+                const long long k = base + j;
+                const int krow = __shfl_sync(kFull, rows_k, j);
+                const int s = static_cast<int>(k % kStages);
+                const uint32_t par = static_cast<uint32_t>((k / kStages) & 1);
+                mbar_wait(bar_empty + 8 * s, par ^ 1u, abort_flag, p.status);
+                uint8_t *stage = smem + kOffStages + s * kStageBytes;
+                if (krow >= 0) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
+                        tma_load_tile(smem_u32(stage), &pool_map, krow, bar_full + 8 * s, policy);
+                        tma_load_tile(smem_u32(stage + kTileBytes), &pool_map, krow + p.Hkv * kP,
+                                      bar_full + 8 * s, policy);
                     }
+                } else {
+                    // Out-of-range page id: flag it and serve zeros.
+                    if (lane == 0 && p.status) atomicOr(p.status, K3DA_STATUS_BAD_PAGE);
+                    uint4 *dst = reinterpret_cast<uint4 *>(stage);
+                    for (int q = lane; q < kStageBytes / 16; q += 32) dst[q] = make_uint4(0, 0, 0, 0);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_full + 8 * s);
                 }
+                __syncwarp();
             }
-            i = seg_end;
         }
         // Drain: every issued load must land before the CTA exits (matters
         // only when a wait gave up and the consumers stopped early).
         if (*abort_flag) {
-            for (long long j = (k > kStages ? k - kStages : 0); j < k; ++j) {
+            for (long long j = (total > kStages ? total - kStages : 0); j < total; ++j) {
                 const int s = static_cast<int>(j % kStages);
                 const uint32_t par = static_cast<uint32_t>((j / kStages) & 1);
                 const unsigned long long t0 = global_ns();
@@ -522,6 +593,7 @@ __global__ void __maxnreg__(144)
                 }
             }
         }
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         return;
     }
 
@@ -548,17 +620,18 @@ __global__ void __maxnreg__(144)
         wk_lo = __bfloat162float(p.k_w[lane]);
         wk_hi = __bfloat162float(p.k_w[lane + 32]);
     }
-    long long k = 0;
-    long long i = beg;
-    for (int u = u0; i < end; ++u) {
-        const long long seg_end = end < ustart[u + 1] ? end : ustart[u + 1];
-        const long long a = i - ustart[u], b = seg_end - ustart[u];
+    long long k = 0;  // pages consumed
+    for (int run = 0; run < nrun; ++run) {
+        const int u = pl->run_u[run];
         const int r = u / p.Hkv, h = u - r * p.Hkv;
-        const int L = lens[r];
-        const bool with_block = a == 0;
+        const int L = pl->lens[r];
+        const int ch = pl->ch[u];
+        const int items = static_cast<int>(pl->ustart[u + 1] - pl->ustart[u]);
+        const int j0 = pl->run_j0[run], j1 = pl->run_j1[run];
+        const bool with_block = j0 == 0;
 
         // ---- stage this unit's q (and block k, v) rows: one round trip.
-        named_bar_sync(1, kConsumerThreads);  // the previous range is done with every tile
+        named_bar_sync(1, kConsumerThreads);  // every tile of the previous run is free
         const char *qkv_rows = reinterpret_cast<const char *>(p.qkv) + static_cast<long long>(r) * p.B * row_w * 2;
         for (int e = ctid; e < p.B * 48; e += kConsumerThreads) {
             const int ti = e / 48, c = e - ti * 48;
@@ -634,88 +707,91 @@ __global__ void __maxnreg__(144)
             }
         }
         named_bar_sync(1, kConsumerThreads);
-
-        RowState st;
-        st.m[0] = st.m[1] = -INFINITY;
-        st.l[0] = st.l[1] = 0.f;
-#pragma unroll
-        for (int nd = 0; nd < 8; ++nd) st.o[nd][0] = st.o[nd][1] = st.o[nd][2] = st.o[nd][3] = 0.f;
         uint32_t qf[4][4];
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
             ldsm_x4(smem_u32(qtile) + swz(rb * 16 + (mi & 1) * 8 + rr, kk * 2 + (mi >> 1)), qf[kk][0], qf[kk][1],
                     qf[kk][2], qf[kk][3]);
 
-        if (with_block && grp == 0 && active)
-            attend_tile<2>(st, qf, smem_u32(bk), smem_u32(bv), 0, p.B, p.scale_log2, lane);
-        const long long pa = a == 0 ? 0 : a - 1, pb = b - 1;
-        for (long long pg = pa; pg < pb; ++pg, ++k) {
-            const int s = static_cast<int>(k % kStages);
-            const uint32_t par = static_cast<uint32_t>((k / kStages) & 1);
-            const bool ok = mbar_wait(bar_full + 8 * s, par, abort_flag, p.status);
-            const long long left = static_cast<long long>(L) - pg * kP - grp * 32;
-            if (active && ok && left > 0) {
-                const int valid = left < 32 ? static_cast<int>(left) : 32;
-                const uint32_t stage = smem_u32(smem + kOffStages + s * kStageBytes);
-                attend_tile<4>(st, qf, stage, stage + kTileBytes, grp * 32, valid, p.scale_log2, lane);
+        for (int jc = j0; jc < j1; ++jc) {
+            RowState st;
+            st.m[0] = st.m[1] = -INFINITY;
+            st.l[0] = st.l[1] = 0.f;
+#pragma unroll
+            for (int nd = 0; nd < 8; ++nd) st.o[nd][0] = st.o[nd][1] = st.o[nd][2] = st.o[nd][3] = 0.f;
+            const int i0 = jc * ch;
+            const int i1 = i0 + ch < items ? i0 + ch : items;
+            if (i0 == 0 && grp == 0 && active)
+                attend_tile<2>(st, qf, smem_u32(bk), smem_u32(bv), 0, p.B, p.scale_log2, lane);
+            for (int pg = (i0 == 0 ? 0 : i0 - 1); pg < i1 - 1; ++pg, ++k) {
+                const int s = static_cast<int>(k % kStages);
+                const uint32_t par = static_cast<uint32_t>((k / kStages) & 1);
+                const bool ok = mbar_wait(bar_full + 8 * s, par, abort_flag, p.status);
+                const int left = L - pg * kP - grp * 32;
+                if (active && ok && left > 0) {
+                    const uint32_t stage = smem_u32(smem + kOffStages + s * kStageBytes);
+                    attend_tile<4>(st, qf, stage, stage + kTileBytes, grp * 32, left < 32 ? left : 32,
+                                   p.scale_log2, lane);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * s);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-        }
 
-        // ---- merge the two key groups, write this (CTA, unit) partial.
-        float *mine = merge + (rb * 36) * 32 + lane;  // [row block][36 values][lane]
-        if (grp == 1 && active) {
+            // ---- merge the two key groups; write the chunk's partial.
+            float *mine = merge + (rb * 36) * 32 + lane;  // [row block][36 values][lane]
+            if (grp == 1 && active) {
 #pragma unroll
-            for (int nd = 0; nd < 8; ++nd)
+                for (int nd = 0; nd < 8; ++nd)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) mine[(nd * 4 + c) * 32] = st.o[nd][c];
-            mine[32 * 32] = st.m[0];
-            mine[33 * 32] = st.m[1];
-            mine[34 * 32] = st.l[0];
-            mine[35 * 32] = st.l[1];
+                    for (int c = 0; c < 4; ++c) mine[(nd * 4 + c) * 32] = st.o[nd][c];
+                mine[32 * 32] = st.m[0];
+                mine[33 * 32] = st.m[1];
+                mine[34 * 32] = st.l[0];
+                mine[35 * 32] = st.l[1];
+            }
+            named_bar_sync(1, kConsumerThreads);
+            if (grp == 0 && active) {
+                float f0[2], f1[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float m1 = mine[(32 + e) * 32];
+                    const float mm = fmaxf(st.m[e], m1);
+                    f0[e] = exp2_approx(st.m[e] - mm);
+                    f1[e] = exp2_approx(m1 - mm);  // 0 when the other group saw no key
+                    st.m[e] = mm;
+                    st.l[e] = st.l[e] * f0[e] + mine[(34 + e) * 32] * f1[e];
+                }
+#pragma unroll
+                for (int nd = 0; nd < 8; ++nd) {
+                    st.o[nd][0] = st.o[nd][0] * f0[0] + mine[(nd * 4 + 0) * 32] * f1[0];
+                    st.o[nd][1] = st.o[nd][1] * f0[0] + mine[(nd * 4 + 1) * 32] * f1[0];
+                    st.o[nd][2] = st.o[nd][2] * f0[1] + mine[(nd * 4 + 2) * 32] * f1[1];
+                    st.o[nd][3] = st.o[nd][3] * f0[1] + mine[(nd * 4 + 3) * 32] * f1[1];
+                }
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    st.l[e] += __shfl_xor_sync(kFull, st.l[e], 1);
+                    st.l[e] += __shfl_xor_sync(kFull, st.l[e], 2);
+                }
+                const long long slot = static_cast<long long>(pl->cstart[u]) + jc;
+                const int ra = rb * 16 + (lane >> 2), rbw = ra + 8;
+                float *ob = p.ws_o + slot * kPartialFloats;
+                const int dq = 2 * (lane & 3);
+#pragma unroll
+                for (int nd = 0; nd < 8; ++nd) {
+                    if (ra < rows)
+                        *reinterpret_cast<float2 *>(ob + ra * kD + nd * 8 + dq) = make_float2(st.o[nd][0], st.o[nd][1]);
+                    if (rbw < rows)
+                        *reinterpret_cast<float2 *>(ob + rbw * kD + nd * 8 + dq) =
+                            make_float2(st.o[nd][2], st.o[nd][3]);
+                }
+                if ((lane & 3) == 0) {
+                    if (ra < rows) p.ws_ml[slot * kRows + ra] = make_float2(st.m[0], st.l[0]);
+                    if (rbw < rows) p.ws_ml[slot * kRows + rbw] = make_float2(st.m[1], st.l[1]);
+                }
+            }
+            named_bar_sync(1, kConsumerThreads);  // the merge area is free again
         }
-        named_bar_sync(1, kConsumerThreads);
-        if (grp == 0 && active) {
-            float f0[2], f1[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const float m1 = mine[(32 + e) * 32];
-                const float mm = fmaxf(st.m[e], m1);
-                f0[e] = exp2_approx(st.m[e] - mm);
-                f1[e] = exp2_approx(m1 - mm);  // 0 when the other group saw no key
-                st.m[e] = mm;
-                st.l[e] = st.l[e] * f0[e] + mine[(34 + e) * 32] * f1[e];
-            }
-#pragma unroll
-            for (int nd = 0; nd < 8; ++nd) {
-                st.o[nd][0] = st.o[nd][0] * f0[0] + mine[(nd * 4 + 0) * 32] * f1[0];
-                st.o[nd][1] = st.o[nd][1] * f0[0] + mine[(nd * 4 + 1) * 32] * f1[0];
-                st.o[nd][2] = st.o[nd][2] * f0[1] + mine[(nd * 4 + 2) * 32] * f1[1];
-                st.o[nd][3] = st.o[nd][3] * f0[1] + mine[(nd * 4 + 3) * 32] * f1[1];
-            }
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                st.l[e] += __shfl_xor_sync(kFull, st.l[e], 1);
-                st.l[e] += __shfl_xor_sync(kFull, st.l[e], 2);
-            }
-            const long long slot = static_cast<long long>(blockIdx.x) + u;
-            const int ra = rb * 16 + (lane >> 2), rbw = ra + 8;
-            float *ob = p.ws_o + slot * kPartialFloats;
-            const int dq = 2 * (lane & 3);
-#pragma unroll
-            for (int nd = 0; nd < 8; ++nd) {
-                if (ra < rows)
-                    *reinterpret_cast<float2 *>(ob + ra * kD + nd * 8 + dq) = make_float2(st.o[nd][0], st.o[nd][1]);
-                if (rbw < rows)
-                    *reinterpret_cast<float2 *>(ob + rbw * kD + nd * 8 + dq) = make_float2(st.o[nd][2], st.o[nd][3]);
-            }
-            if ((lane & 3) == 0) {
-                if (ra < rows) p.ws_ml[slot * kRows + ra] = make_float2(st.m[0], st.l[0]);
-                if (rbw < rows) p.ws_ml[slot * kRows + rbw] = make_float2(st.m[1], st.l[1]);
-            }
-        }
-        i = seg_end;
     }
     // Let the combine grid start launching; it waits for this grid to finish.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -723,33 +799,34 @@ __global__ void __maxnreg__(144)
 
 // --------------------------------------------------------------- combine --
 //
-// One CTA per (unit, 4 query rows), 256 threads: thread = (row, segment
-// lane sg of 8, 8 dims).  Each thread merges the unit's partials sg, sg+8,
-// ... online; the 8 segment lanes then merge in fixed order through shared
-// memory, so the result does not depend on timing.  Launched as a
-// programmatic dependent of the split pass: the prologue overlaps its tail
-// and griddepcontrol.wait orders the partial reads after it.
+// One CTA per (unit, 2 query rows), 256 threads: thread = (row, 8 dims,
+// chunk lane sg of 16), the 16 chunk lanes of one (row, dims) sitting in one
+// half-warp.  Lane sg folds the unit's chunk partials sg, sg+16, ... online;
+// the lanes then merge by a fixed butterfly of shuffles, so the result
+// depends on nothing but the unit's own chunks.  Launched as a programmatic
+// dependent of the split pass: the prologue overlaps its tail and
+// griddepcontrol.wait orders the partial reads after it.
+constexpr int kCombineRows = 2;
+constexpr int kCombineLanes = 16;
+
 __global__ void __launch_bounds__(256) k3da_combine_kernel(const __grid_constant__ Params p) {
-    __shared__ long long ustart[kMaxUnits + 1];
-    __shared__ int lens[kMaxR];
-    __shared__ float red[4][8][10];
-    build_partition(p, lens, ustart, false);
+    __shared__ Plan pl;
+    build_plan(p, &pl, -1, 1, false);
     __syncthreads();
-    const int u = blockIdx.x / (kRows / 4);
-    const int row = (blockIdx.x - u * (kRows / 4)) * 4 + (threadIdx.x >> 6);
-    const int sg = (threadIdx.x >> 3) & 7, dc = threadIdx.x & 7;
+    const int per_unit = kRows / kCombineRows;
+    const int u = blockIdx.x / per_unit;
+    const int row = (blockIdx.x - u * per_unit) * kCombineRows + (threadIdx.x >> 7);
+    const int dc = (threadIdx.x >> 4) & 7, sg = threadIdx.x & (kCombineLanes - 1);
     const int rows = kG * p.B;
-    const int U = p.R * p.Hkv;
-    const long long W = ustart[U];
-    const long long C = W < p.grid ? W : p.grid;
-    const int c0 = cta_of_item(ustart[u], W, C);
-    const int c1 = cta_of_item(ustart[u + 1] - 1, W, C);
+    const int nch = pl.nch[u];
+    const long long slot0 = pl.cstart[u];
     asm volatile("griddepcontrol.wait;" ::: "memory");
     float m = -INFINITY, l = 0.f;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (row < rows) {
-        for (int c = c0 + sg; c <= c1; c += 8) {
-            const long long slot = static_cast<long long>(c) + u;
+#pragma unroll 4
+        for (int j = sg; j < nch; j += kCombineLanes) {
+            const long long slot = slot0 + j;
             const float2 ml = p.ws_ml[slot * kRows + row];
             const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + slot * kPartialFloats + row * kD + dc * 8);
             const float4 v0 = src[0], v1 = src[1];
@@ -767,44 +844,32 @@ __global__ void __launch_bounds__(256) k3da_combine_kernel(const __grid_constant
             acc[7] = acc[7] * fo + v1.w * fn;
         }
     }
-    // Fixed-order merge of the 8 segment lanes, one dim chunk at a time.
-    const int rl = threadIdx.x >> 6;
-    float outv[8];
-    for (int d = 0; d < 8; ++d) {
-        __syncthreads();
-        if (dc == d) {
-            red[rl][sg][0] = m;
-            red[rl][sg][1] = l;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) red[rl][sg][2 + j] = acc[j];
+    for (int off = kCombineLanes / 2; off >= 1; off >>= 1) {
+        const float m2 = __shfl_xor_sync(kFull, m, off);
+        const float l2 = __shfl_xor_sync(kFull, l, off);
+        const float mm = fmaxf(m, m2);
+        const bool none = mm == -INFINITY;  // neither lane holds a chunk
+        const float fa = none ? 0.f : exp2_approx(m - mm);
+        const float fb = none ? 0.f : exp2_approx(m2 - mm);
+        l = l * fa + l2 * fb;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float a2 = __shfl_xor_sync(kFull, acc[j], off);
+            acc[j] = acc[j] * fa + a2 * fb;
         }
-        __syncthreads();
-        if (dc == d && sg == 0) {
-            float M = -INFINITY;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) M = fmaxf(M, red[rl][q][0]);
-            float lt = 0.f, at[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float f = exp2_approx(red[rl][q][0] - M);  // 0 for empty lanes
-                lt = fmaf(red[rl][q][1], f, lt);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) at[j] = fmaf(red[rl][q][2 + j], f, at[j]);
-            }
-            const float inv = 1.0f / lt;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) outv[j] = at[j] * inv;
-        }
+        m = mm;
     }
     if (sg == 0 && row < rows) {
+        const float inv = 1.0f / l;
         const int r = u / p.Hkv, h = u - r * p.Hkv;
         const int g = row / p.B, ti = row - g * p.B;
         const long long t = static_cast<long long>(r) * p.B + ti;
         uint4 packed;
-        packed.x = pack_bf16(outv[0], outv[1]);
-        packed.y = pack_bf16(outv[2], outv[3]);
-        packed.z = pack_bf16(outv[4], outv[5]);
-        packed.w = pack_bf16(outv[6], outv[7]);
+        packed.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+        packed.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+        packed.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+        packed.w = pack_bf16(acc[6] * inv, acc[7] * inv);
         *reinterpret_cast<uint4 *>(p.out + t * (static_cast<long long>(p.Hq) * kD) +
                                    static_cast<long long>(h * kG + g) * kD + dc * 8) = packed;
     }
@@ -872,9 +937,16 @@ int configure_device(int dev, DeviceConfig *cfg) {
 
 bool supported_heads(int hq, int hkv) { return (hq == 6 && hkv == 1) || (hq == 24 && hkv == 4); }
 
-size_t workspace_for(int sms) {
-    const size_t slots = static_cast<size_t>(sms) * kMaxCtasPerSm + kMaxUnits;
-    return slots * (kPartialFloats * sizeof(float) + kRows * sizeof(float2));
+// Chunks a unit can have: at most kChunkSplits, or ceil(items/kChunkMax)
+// once chunks reach kChunkMax items; items <= page_stride + 1.
+size_t workspace_slots(int R, int Hkv, int page_stride) {
+    const long long by_len = (static_cast<long long>(page_stride) + 1 + kChunkMax - 1) / kChunkMax;
+    const long long per_unit = by_len > kChunkSplits ? by_len : kChunkSplits;
+    return static_cast<size_t>(R) * Hkv * static_cast<size_t>(per_unit);
+}
+
+size_t workspace_for(int R, int Hkv, int page_stride) {
+    return workspace_slots(R, Hkv, page_stride) * (kPartialFloats * sizeof(float) + kRows * sizeof(float2));
 }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -908,7 +980,7 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
     DeviceConfig cfg;
     int rc = configure_device(dev, &cfg);
     if (rc != K3DA_OK) return rc;
-    if (workspace_bytes < workspace_for(cfg.sms)) return K3DA_EWORKSPACE;
+    if (workspace_bytes < workspace_for(R, Hkv, page_stride)) return K3DA_EWORKSPACE;
 
     CUtensorMap map;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD),
@@ -930,7 +1002,7 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
     prm.positions = positions;
     prm.q_w = static_cast<const __nv_bfloat16 *>(q_norm_w);
     prm.k_w = static_cast<const __nv_bfloat16 *>(k_norm_w);
-    const size_t slots = static_cast<size_t>(cfg.sms) * kMaxCtasPerSm + kMaxUnits;
+    const size_t slots = workspace_slots(R, Hkv, page_stride);
     prm.ws_o = static_cast<float *>(workspace);
     prm.ws_ml = reinterpret_cast<float2 *>(static_cast<float *>(workspace) + slots * kPartialFloats);
     prm.status = status;
@@ -959,7 +1031,7 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
     // launch and prologue overlap the split pass's tail.
     cudaLaunchConfig_t lc;
     memset(&lc, 0, sizeof lc);
-    lc.gridDim = dim3(static_cast<unsigned>(R * Hkv * (kRows / 4)));
+    lc.gridDim = dim3(static_cast<unsigned>(R * Hkv * (kRows / kCombineRows)));
     lc.blockDim = dim3(256);
     lc.dynamicSmemBytes = 0;
     lc.stream = st;
@@ -977,15 +1049,12 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
 
 extern "C" {
 
-size_t k3da_workspace_bytes(int num_requests, int block_len, int num_q_heads, int num_kv_heads, int device) {
+size_t k3da_workspace_bytes(int num_requests, int block_len, int num_q_heads, int num_kv_heads,
+                            int page_stride) {
     if (num_requests < 1 || num_requests > kMaxR || block_len < 1 || block_len > kMaxB ||
-        !supported_heads(num_q_heads, num_kv_heads))
+        !supported_heads(num_q_heads, num_kv_heads) || page_stride < 1)
         return 0;
-    int dev = device;
-    if (dev < 0 && cudaGetDevice(&dev) != cudaSuccess) return 0;
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return workspace_for(sms);
+    return workspace_for(num_requests, num_kv_heads, page_stride);
 }
 
 int k3da_attn(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, const int32_t *page_table,

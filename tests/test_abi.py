@@ -100,9 +100,17 @@ def test_qknorm_host_checks(lib, over):
 
 
 def test_workspace_query_refuses_bad_sizes(lib):
-    assert lib.k3da_workspace_bytes(0, 8, 6, 1, 0) == 0
-    assert lib.k3da_workspace_bytes(8, 9, 6, 1, 0) == 0
-    assert lib.k3da_workspace_bytes(8, 8, 6, 2, 0) == 0
+    assert lib.k3da_workspace_bytes(0, 8, 6, 1, 32) == 0
+    assert lib.k3da_workspace_bytes(8, 9, 6, 1, 32) == 0
+    assert lib.k3da_workspace_bytes(8, 8, 6, 2, 32) == 0
+    assert lib.k3da_workspace_bytes(8, 8, 6, 1, 0) == 0
+
+
+def test_workspace_size_depends_on_shapes_only(lib):
+    small = lib.k3da_workspace_bytes(1, 8, 6, 1, 32)
+    assert small > 0
+    assert lib.k3da_workspace_bytes(8, 8, 24, 4, 32) == 32 * small
+    assert lib.k3da_workspace_bytes(8, 8, 24, 4, 2048) > lib.k3da_workspace_bytes(8, 8, 24, 4, 32)
 
 
 def test_product_path_does_not_touch_the_oracle():

@@ -21,7 +21,7 @@ def fresh_out(case):
 def test_reruns_are_bit_identical_and_pool_untouched():
     case = workloads.heads_24_4(device="cuda")
     pool_before = case.pool.clone()
-    ws = k3da.alloc_workspace(case.R, case.B, case.Hq, case.Hkv)
+    ws = k3da.case_workspace(case)
     a = k3da.run_case(case, workspace=ws).clone()
     for _ in range(5):
         ws.fill_(0xFF)  # NaN-pattern workspace between calls
@@ -104,7 +104,7 @@ def test_device_range_checks_flag_and_stay_finite():
 
 def test_host_side_refusals_raise():
     case = workloads.tiny(device="cuda")
-    ws = k3da.alloc_workspace(case.R, case.B, case.Hq, case.Hkv)
+    ws = k3da.case_workspace(case)
     with pytest.raises(k3da.K3daError):
         k3da.run_case(case, workspace=ws[:16])  # too small
     with pytest.raises(k3da.K3daError):
@@ -115,7 +115,7 @@ def test_host_side_refusals_raise():
 @pytest.mark.parametrize("maker", [workloads.mixed_8x8, workloads.heads_24_4])
 def test_graph_replay_with_rewritten_inputs(maker):
     case = maker(device="cuda")
-    ws = k3da.alloc_workspace(case.R, case.B, case.Hq, case.Hkv)
+    ws = k3da.case_workspace(case)
     out = fresh_out(case)
     k3da.run_case(case, out=out, workspace=ws)  # first call outside capture
     torch.cuda.synchronize()

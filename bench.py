@@ -390,7 +390,8 @@ def run_ours(args, world, rank):
             "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",
             "data": "synthetic (seeded N(0,1) bf16 pool/qkv, random page permutation)",
-            "config": config_of(case, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
+            "config": config_of(case, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                                       "split_ctas": k3da.split_grid(dev.index)}),
             "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clock_info,
             "median_call_us": statistics.median(call_ms) * 1e3,
             "p10_p90_call_us": [sorted(call_ms)[int(0.1 * (K - 1))] * 1e3,

@@ -141,6 +141,13 @@ int k3da_attn_qknorm(void *out, const void *qkv, const void *kv_pool, int64_t nu
  */
 int k3da_set_phase_event(void *event);
 
+/*
+ * CTAs the split pass launches on `device` (-1 = current): SM count times
+ * the CTAs per SM its resources allow.  Configures the device like a first
+ * call does.  Returns 0 when the device cannot be configured.
+ */
+int k3da_split_grid(int device);
+
 /* Static description of a k3da_error or K3DA_STATUS_* bit set. */
 const char *k3da_error_string(int code);
 

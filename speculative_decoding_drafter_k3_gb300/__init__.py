@@ -35,8 +35,8 @@ _lib = None
 OK, EINVAL, EUNSUPPORTED, ECUDA, EWORKSPACE = 0, -1, -2, -3, -4
 STATUS_BAD_LENGTH, STATUS_BAD_PAGE, STATUS_TIMEOUT = 1, 2, 4
 POS_I32, POS_I64 = 0, 1
-EXPORTED = ["k3da_workspace_bytes", "k3da_attn", "k3da_attn_qknorm", "k3da_set_phase_event",
-            "k3da_error_string", "k3da_version"]
+EXPORTED = ["k3da_workspace_bytes", "k3da_attn", "k3da_attn_qknorm", "k3da_split_grid",
+            "k3da_set_phase_event", "k3da_error_string", "k3da_version"]
 
 
 class K3daError(ValueError):
@@ -69,6 +69,8 @@ def load_library():
         lib.k3da_attn_qknorm.restype = c_int
         lib.k3da_error_string.argtypes = [c_int]
         lib.k3da_error_string.restype = ctypes.c_char_p
+        lib.k3da_split_grid.argtypes = [c_int]
+        lib.k3da_split_grid.restype = c_int
         lib.k3da_set_phase_event.argtypes = [vp]
         lib.k3da_set_phase_event.restype = c_int
         lib.k3da_version.argtypes = []
@@ -203,3 +205,8 @@ def set_phase_event(event):
     else:
         handle = ctypes.c_void_p(event.cuda_event)
     _check(load_library().k3da_set_phase_event(handle), "k3da_set_phase_event")
+
+
+def split_grid(device: int = -1) -> int:
+    """CTAs the split pass launches on ``device`` (SMs x CTAs per SM)."""
+    return int(load_library().k3da_split_grid(device))

@@ -462,7 +462,7 @@ __device__ __forceinline__ void attend_tile(RowState &st, const uint32_t (&qf)[4
 // `row` of a swizzled tile.  w_lo / w_hi are the norm weights of those dims.
 template <bool QKNORM>
 __device__ __forceinline__ void prep_row(uint8_t *tile, int row, float x_lo, float x_hi, float w_lo,
-                                         float w_hi, float eps, float2 cs, int lane) {
+                                         float w_hi, float eps, float2 cs, int lane, int row2 = -1) {
     float y_lo = x_lo, y_hi = x_hi;
     if (QKNORM) {
         float ss = x_lo * x_lo + x_hi * x_hi;
@@ -474,9 +474,13 @@ __device__ __forceinline__ void prep_row(uint8_t *tile, int row, float x_lo, flo
         y_lo = n_lo * cs.x - n_hi * cs.y;
         y_hi = n_hi * cs.x + n_lo * cs.y;
     }
-    *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, lane >> 3) + (lane & 7) * 2) = __float2bfloat16_rn(y_lo);
-    *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, 4 + (lane >> 3)) + (lane & 7) * 2) =
-        __float2bfloat16_rn(y_hi);
+    const __nv_bfloat16 b_lo = __float2bfloat16_rn(y_lo), b_hi = __float2bfloat16_rn(y_hi);
+    *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, lane >> 3) + (lane & 7) * 2) = b_lo;
+    *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, 4 + (lane >> 3)) + (lane & 7) * 2) = b_hi;
+    if (row2 >= 0) {
+        *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row2, lane >> 3) + (lane & 7) * 2) = b_lo;
+        *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row2, 4 + (lane >> 3)) + (lane & 7) * 2) = b_hi;
+    }
 }
 
 __device__ __forceinline__ void zero_row(uint8_t *tile, int row, int lane) {
@@ -797,6 +801,563 @@ __global__ void __launch_bounds__(kThreads, 2)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---------------------------------------------------- tcgen05 split pass --
+//
+// The same work plan, with the two contractions on the 5th-generation tensor
+// cores.  Warps 0..3 own the four 32-lane quarters of tensor memory (TMEM):
+// query row rho = 12*q + l (q = rho / 12 < 4, l < 12) is copied into Q-tile
+// rows (and TMEM lanes) 32*q + l and 32*q + 16 + l; the thread of the first
+// lane handles keys 0..31 of each page and the thread of the second keys
+// 32..63, so a row's softmax costs two threads half a page each and one
+// shuffle to share the row maximum.  Warp 4 streams K/V pages with TMA as
+// before; lane 0 of warp 5 issues the MMAs:
+//   S[b] (128 x 64 fp32, TMEM cols 64b..)  = Q (128 x 64, smem) . K_page^T
+//   O    (128 x 64 fp32, TMEM cols 128..) += P[b] (bf16, TMEM cols 192+32b..) . V_page
+// with two S buffers so the next page's QK^T overlaps this page's softmax.
+// The softmax keeps a per-row exponent base m; P = 2^(s*scale*log2e - m) is
+// written as bf16 to TMEM buffer P[b] (cols 192 + 32b; each lane's other
+// half of the keys as zeros; kept apart from S[b] so that the next QK^T into
+// S[b] never overwrites a P the previous PV may still be reading) and
+// becomes the A operand of the PV MMA, so each of a row's two lanes
+// accumulates its half of P.V; the halves are added when the chunk's
+// partial is written.  O is only rescaled when a row's maximum passes m by
+// more than 8 (log2 units; P <= 256 is exact enough in bf16 and fp32), so
+// the common path never touches O.
+namespace tc {
+#ifndef K3DA_TC_STAGES
+#define K3DA_TC_STAGES 4
+#endif
+constexpr int kStages = K3DA_TC_STAGES;
+constexpr int kRowWarps = 4;
+constexpr int kRowThreads = 32 * kRowWarps;
+constexpr int kRowsPerQuarter = 12;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kThreads = 32 * 6;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColO = 128;
+constexpr uint32_t kColP = 192;  // P[b] at kColP + 32*b (bf16 pairs), apart from S[b]
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Shared memory (offsets from a 1024-byte aligned base).
+constexpr int kOffStages = 0;                        // kStages x (K 8 KB + V 8 KB)
+constexpr int kOffQ = kStages * kStageBytes;         // 128 rows x 128 B, 128B swizzle
+constexpr int kOffBlkK = kOffQ + 128 * 128;          // 64 rows x 128 B
+constexpr int kOffBlkV = kOffBlkK + 64 * 128;        // 64 rows x 128 B
+constexpr int kOffRaw = kOffBlkV + 64 * 128;         // raw q [8][6][64], k [8][64], v [8][64]
+constexpr int kOffTrig = kOffRaw + kMaxB * (kG + 2) * kD * 2;  // [8][32] float2
+constexpr int kOffPlan = kOffTrig + kMaxB * 32 * 8;
+constexpr int kNumBars = 2 * kStages + 7;  // full, empty, s_full[2], p_full[2], o_done, q_ready, done
+constexpr int kOffBar = kOffPlan + 1536;
+constexpr int kOffTaddr = kOffBar + kNumBars * 8;
+constexpr int kOffFlag = kOffTaddr + 8;
+constexpr int kSmemUsed = kOffFlag + 16;
+constexpr int kSmemBytes = kSmemUsed + 1024;
+static_assert(kOffQ % 1024 == 0 && kOffBlkK % 1024 == 0 && kOffBlkV % 1024 == 0, "SW128 tiles need 1 KB alignment");
+static_assert(kOffBar % 8 == 0 && kOffPlan % 8 == 0, "mbarrier / int64 alignment");
+
+// Instruction descriptor of kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9 = 1, 10-12 = 1), K-major A and B unless bit 16 makes B
+// MN-major, N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kIdescPV = kIdescQK | (1u << 16);
+
+// Shared-memory matrix descriptor of a tile stored in 128-byte rows with the
+// 128-byte swizzle (8-row, 1 KB atoms): start address >> 4 (bits 0-13),
+// leading byte offset 16 B >> 4 (bits 16-29, unused here), stride byte
+// offset 1 KB >> 4 between 8-row groups (bits 32-45), descriptor version 1
+// (bits 46-47), layout SWIZZLE_128B = 2 (bits 61-63).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t smem_addr) {
+    return static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 64 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+}  // namespace tc
+
+template <bool QKNORM>
+__global__ void __launch_bounds__(tc::kThreads, 2)
+    k3da_tc_kernel(const __grid_constant__ CUtensorMap pool_map, const __grid_constant__ Params p) {
+    constexpr auto kStages = tc::kStages;
+    constexpr auto kRowWarps = tc::kRowWarps;
+    constexpr auto kRowThreads = tc::kRowThreads;
+    constexpr auto kRowsPerQuarter = tc::kRowsPerQuarter;
+    constexpr auto kProducerWarp = tc::kProducerWarp;
+    constexpr auto kMmaWarp = tc::kMmaWarp;
+    constexpr auto kThreads = tc::kThreads;
+    constexpr auto kTmemCols = tc::kTmemCols;
+    constexpr auto kColO = tc::kColO;
+    constexpr auto kColP = tc::kColP;
+    constexpr auto kRescaleThreshold = tc::kRescaleThreshold;
+    constexpr auto kOffStages = tc::kOffStages;
+    constexpr auto kOffQ = tc::kOffQ;
+    constexpr auto kOffBlkK = tc::kOffBlkK;
+    constexpr auto kOffBlkV = tc::kOffBlkV;
+    constexpr auto kOffRaw = tc::kOffRaw;
+    constexpr auto kOffTrig = tc::kOffTrig;
+    constexpr auto kOffPlan = tc::kOffPlan;
+    constexpr auto kNumBars = tc::kNumBars;
+    constexpr auto kOffBar = tc::kOffBar;
+    constexpr auto kOffTaddr = tc::kOffTaddr;
+    constexpr auto kOffFlag = tc::kOffFlag;
+    constexpr auto kIdescQK = tc::kIdescQK;
+    constexpr auto kIdescPV = tc::kIdescPV;
+    using tc::desc_sw128;
+    using tc::mma_ss;
+    using tc::mma_ts;
+    using tc::mma_commit;
+    using tc::fence_before;
+    using tc::fence_after;
+    using tc::tmem_ld64;
+    using tc::tmem_st32;
+    using tc::tmem_wait_st;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Plan *pl = reinterpret_cast<Plan *>(smem + kOffPlan);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffFlag);
+    uint32_t *taddr_slot = reinterpret_cast<uint32_t *>(smem + kOffTaddr);
+    const uint32_t bars = smem_u32(smem + kOffBar);
+    const uint32_t bar_full = bars, bar_empty = bars + 8 * kStages;
+    const uint32_t bar_sfull = bars + 16 * kStages, bar_pfull = bar_sfull + 16;
+    const uint32_t bar_odone = bar_pfull + 16, bar_qready = bar_odone + 8, bar_done = bar_qready + 8;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    build_plan(p, pl, blockIdx.x, p.grid, blockIdx.x == 0);
+    {
+        // Q and block tiles start as zeros: rows without a query row or a
+        // block token stay zero for the whole kernel.
+        uint4 *z = reinterpret_cast<uint4 *>(smem + kOffQ);
+        for (int e = threadIdx.x; e < (128 * 128 + 2 * 64 * 128) / 16; e += kThreads) z[e] = make_uint4(0, 0, 0, 0);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        mbar_init(bar_sfull, 1);
+        mbar_init(bar_sfull + 8, 1);
+        mbar_init(bar_pfull, kRowWarps);
+        mbar_init(bar_pfull + 8, kRowWarps);
+        mbar_init(bar_odone, 1);
+        mbar_init(bar_qready, kRowWarps);
+        mbar_init(bar_done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(taddr_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *taddr_slot;
+    const int nrun = pl->nrun;
+
+    if (warp == kProducerWarp && nrun > 0) {
+        // ------------------------------------------------ producer warp --
+        uint64_t policy;
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+        const int total = pl->run_pq[nrun];
+        auto resolve = [&](int q) -> int {
+            if (q >= total) return -1;
+            int k = 0;
+            while (pl->run_pq[k + 1] <= q) ++k;
+            const int u = pl->run_u[k];
+            const int r = u / p.Hkv, h = u - r * p.Hkv;
+            const int page = __ldg(p.page_table + static_cast<long long>(r) * p.page_stride + pl->run_p0[k] +
+                                   (q - pl->run_pq[k]));
+            if (page < 0 || page >= p.num_pages) return -1;  // served as zeros, flagged
+            return ((page * 2 + 0) * p.Hkv + h) * kP;
+        };
+        int next = resolve(lane);
+        for (int base = 0; base < total; base += 32) {
+            const int rows_k = next;
+            next = resolve(base + 32 + lane);
+            const int cnt = total - base < 32 ? total - base : 32;
+            for (int j = 0; j < cnt; ++j) {
+                const long long k = base + j;
+                const int krow = __shfl_sync(kFull, rows_k, j);
+                const int s = static_cast<int>(k % kStages);
+                const uint32_t par = static_cast<uint32_t>((k / kStages) & 1);
+                mbar_wait(bar_empty + 8 * s, par ^ 1u, abort_flag, p.status);
+                uint8_t *stage = smem + kOffStages + s * kStageBytes;
+                if (krow >= 0) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
+                        tma_load_tile(smem_u32(stage), &pool_map, krow, bar_full + 8 * s, policy);
+                        tma_load_tile(smem_u32(stage + kTileBytes), &pool_map, krow + p.Hkv * kP, bar_full + 8 * s,
+                                      policy);
+                    }
+                } else {
+                    if (lane == 0 && p.status) atomicOr(p.status, K3DA_STATUS_BAD_PAGE);
+                    uint4 *dst = reinterpret_cast<uint4 *>(stage);
+                    for (int q = lane; q < kStageBytes / 16; q += 32) dst[q] = make_uint4(0, 0, 0, 0);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_full + 8 * s);
+                }
+                __syncwarp();
+            }
+        }
+        if (*abort_flag) {
+            for (long long j = (total > kStages ? total - kStages : 0); j < total; ++j) {
+                const int s = static_cast<int>(j % kStages);
+                const uint32_t par = static_cast<uint32_t>((j / kStages) & 1);
+                const unsigned long long t0 = global_ns();
+                while (!mbar_try_wait(bar_full + 8 * s, par) && global_ns() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+    } else if (warp == kMmaWarp && nrun > 0) {
+        // ---------------------------------------------------- MMA warp --
+        // Items run in order; the QK^T of item i+1 is issued before the PV
+        // of item i (within a run), so it overlaps item i's softmax.
+        const uint64_t q_desc = desc_sw128(smem_u32(smem + kOffQ));
+        const uint64_t bk_desc = desc_sw128(smem_u32(smem + kOffBlkK));
+        const uint64_t bv_desc = desc_sw128(smem_u32(smem + kOffBlkV));
+        long long it = 0, kr = 0;
+        bool pend = false;
+        int pend_b = 0, pend_s = 0;
+        bool pend_page = false, pend_first = false;
+        long long pend_it = 0;
+        auto issue_pv = [&]() {
+            mbar_wait(bar_pfull + 8 * pend_b, static_cast<uint32_t>((pend_it >> 1) & 1), abort_flag, p.status);
+            fence_after();
+            if (lane == 0) {
+                const uint64_t v_desc =
+                    pend_page ? desc_sw128(smem_u32(smem + kOffStages + pend_s * kStageBytes + kTileBytes)) : bv_desc;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ts(tmem + kColO, tmem + kColP + 32u * pend_b + 8u * kk, v_desc + ((kk * 2048) >> 4), kIdescPV,
+                           (kk > 0 || !pend_first) ? 1u : 0u);
+                mma_commit(bar_odone);
+                if (pend_page) mma_commit(bar_empty + 8 * pend_s);
+            }
+            __syncwarp();
+        };
+        for (int rn = 0; rn < nrun; ++rn) {
+            const int u = pl->run_u[rn];
+            const int ch = pl->ch[u];
+            const int items = static_cast<int>(pl->ustart[u + 1] - pl->ustart[u]);
+            mbar_wait(bar_qready, static_cast<uint32_t>(rn & 1), abort_flag, p.status);
+            fence_after();
+            for (int jc = pl->run_j0[rn]; jc < pl->run_j1[rn]; ++jc) {
+                const int i0 = jc * ch;
+                const int i1 = i0 + ch < items ? i0 + ch : items;
+                for (int item = i0; item < i1; ++item) {
+                    const int b = static_cast<int>(it & 1);
+                    const bool is_page = item > 0;
+                    const int s = static_cast<int>(kr % kStages);
+                    if (is_page) {
+                        mbar_wait(bar_full + 8 * s, static_cast<uint32_t>((kr / kStages) & 1), abort_flag, p.status);
+                        fence_after();
+                    }
+                    if (lane == 0) {
+                        const uint64_t k_desc = is_page ? desc_sw128(smem_u32(smem + kOffStages + s * kStageBytes))
+                                                        : bk_desc;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tmem + 64u * b, q_desc + ((kk * 32) >> 4), k_desc + ((kk * 32) >> 4), kIdescQK,
+                                   kk > 0 ? 1u : 0u);
+                        mma_commit(bar_sfull + 8 * b);
+                    }
+                    __syncwarp();
+                    if (pend) issue_pv();
+                    pend = true;
+                    pend_b = b;
+                    pend_s = s;
+                    pend_page = is_page;
+                    pend_first = item == i0;
+                    pend_it = it;
+                    ++it;
+                    if (is_page) ++kr;
+                }
+            }
+            if (pend) issue_pv();
+            pend = false;
+        }
+        if (lane == 0) mma_commit(bar_done);
+        __syncwarp();
+        const unsigned long long t0 = global_ns();
+        while (!mbar_try_wait(bar_done, 0) && global_ns() - t0 < kWaitLimitNs) {
+        }
+    } else if (warp < kRowWarps && nrun > 0) {
+        // ------------------------------------------- softmax / row warps --
+        const int t = threadIdx.x;
+        const int q = warp;
+        const int half = lane >> 4;               // key half of this lane
+        const int l16 = lane & 15;
+        const int rho = l16 < kRowsPerQuarter ? q * kRowsPerQuarter + l16 : 1 << 20;
+        const int rows = kG * p.B;
+        const bool active = rho < rows;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+        uint8_t *qtile = smem + kOffQ;
+        uint8_t *bk = smem + kOffBlkK;
+        uint8_t *bv = smem + kOffBlkV;
+        uint8_t *raw_q = smem + kOffRaw;
+        uint8_t *raw_k = raw_q + kMaxB * kG * kD * 2;
+        uint8_t *raw_v = raw_k + kMaxB * kD * 2;
+        float2 *trig = reinterpret_cast<float2 *>(smem + kOffTrig);
+        const long long row_w = static_cast<long long>(p.Hq + 2 * p.Hkv) * kD;
+        float wq_lo = 1.f, wq_hi = 1.f, wk_lo = 1.f, wk_hi = 1.f;
+        if (QKNORM) {
+            wq_lo = __bfloat162float(p.q_w[lane]);
+            wq_hi = __bfloat162float(p.q_w[lane + 32]);
+            wk_lo = __bfloat162float(p.k_w[lane]);
+            wk_hi = __bfloat162float(p.k_w[lane + 32]);
+        }
+        long long it = 0, kr = 0;
+        for (int rn = 0; rn < nrun; ++rn) {
+            const int u = pl->run_u[rn];
+            const int r = u / p.Hkv, h = u - r * p.Hkv;
+            const int L = pl->lens[r];
+            const int ch = pl->ch[u];
+            const int items = static_cast<int>(pl->ustart[u + 1] - pl->ustart[u]);
+            const int j0 = pl->run_j0[rn], j1 = pl->run_j1[rn];
+            const bool with_block = j0 == 0;
+
+            // ---- stage and build this unit's Q (and block K, V) tiles.
+            named_bar_sync(1, kRowThreads);
+            const char *qkv_rows = reinterpret_cast<const char *>(p.qkv) + static_cast<long long>(r) * p.B * row_w * 2;
+            for (int e = t; e < p.B * 48; e += kRowThreads) {
+                const int ti = e / 48, c = e - ti * 48;
+                cp_async16(smem_u32(raw_q) + ti * 768 + c * 16,
+                           qkv_rows + ti * row_w * 2 + static_cast<long long>(h) * 768 + c * 16);
+            }
+            if (with_block) {
+                for (int e = t; e < p.B * 16; e += kRowThreads) {
+                    const int ti = e >> 4, c = e & 15;
+                    const long long head = c < 8 ? p.Hq + h : p.Hq + p.Hkv + h;
+                    cp_async16(smem_u32(c < 8 ? raw_k : raw_v) + ti * 128 + (c & 7) * 16,
+                               qkv_rows + ti * row_w * 2 + head * 128 + (c & 7) * 16);
+                }
+            }
+            if (QKNORM) {
+                long long pos[2] = {0, 0};
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const int e = t + k2 * kRowThreads;
+                    if (e < p.B * 32) {
+                        const long long tok = static_cast<long long>(r) * p.B + (e >> 5);
+                        pos[k2] = p.pos_i64 ? reinterpret_cast<const long long *>(p.positions)[tok]
+                                            : reinterpret_cast<const int *>(p.positions)[tok];
+                    }
+                }
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const int e = t + k2 * kRowThreads;
+                    if (e < p.B * 32) {
+                        const double theta = static_cast<double>(pos[k2]) * p.inv_freq[e & 31];
+                        const double turns = rint(theta * 0.15915494309189535);
+                        double red = fma(-turns, 6.283185307179586, theta);
+                        red = fma(-turns, 2.4492935982947064e-16, red);
+                        float sn, cs;
+                        sincosf(static_cast<float>(red), &sn, &cs);
+                        trig[e] = make_float2(cs, sn);
+                    }
+                }
+            }
+            cp_async_wait_all();
+            named_bar_sync(1, kRowThreads);
+            const int prep_rows = with_block ? kRows + 2 * kMaxB : kRows;
+            for (int pr = warp; pr < prep_rows; pr += kRowWarps) {
+                if (pr < kRows) {
+                    if (pr < rows) {
+                        const int g = pr / p.B, ti = pr - g * p.B;
+                        const int idx = (ti * kG + g) * kD;
+                        const int trow = (pr / kRowsPerQuarter) * 32 + pr % kRowsPerQuarter;
+                        prep_row<QKNORM>(qtile, trow, bf16_at(raw_q, idx + lane), bf16_at(raw_q, idx + lane + 32),
+                                         wq_lo, wq_hi, p.eps, QKNORM ? trig[ti * 32 + lane] : make_float2(1.f, 0.f),
+                                         lane, trow + 16);
+                    }
+                } else if (pr < kRows + kMaxB) {
+                    const int j = pr - kRows;
+                    if (j < p.B)
+                        prep_row<QKNORM>(bk, j, bf16_at(raw_k, j * kD + lane), bf16_at(raw_k, j * kD + lane + 32),
+                                         wk_lo, wk_hi, p.eps, QKNORM ? trig[j * 32 + lane] : make_float2(1.f, 0.f),
+                                         lane);
+                } else {
+                    const int j = pr - kRows - kMaxB;
+                    if (j < p.B)
+                        prep_row<false>(bv, j, bf16_at(raw_v, j * kD + lane), bf16_at(raw_v, j * kD + lane + 32),
+                                        1.f, 1.f, 0.f, make_float2(1.f, 0.f), lane);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_qready);
+
+            float m_used = 0.f, lsum = 0.f;
+            for (int jc = j0; jc < j1; ++jc) {
+                const int i0 = jc * ch;
+                const int i1 = i0 + ch < items ? i0 + ch : items;
+                for (int item = i0; item < i1; ++item) {
+                    const int b = static_cast<int>(it & 1);
+                    const bool is_page = item > 0;
+                    const int s = static_cast<int>(kr % kStages);
+                    int valid = p.B;
+                    if (is_page) {
+                        const int left = L - (item - 1) * kP;
+                        valid = left < kP ? left : kP;
+                    }
+                    mbar_wait(bar_sfull + 8 * b, static_cast<uint32_t>((it >> 1) & 1), abort_flag, p.status);
+                    fence_after();
+                    uint32_t sr[64];
+                    tmem_ld64(tmem + lane_off + 64u * b, sr);
+                    // This lane's half of the keys.
+                    float sv[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(half ? sr[32 + j] : sr[j]);
+                    if (valid < kP) {
+                        const int lim = valid - 32 * half;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) sv[j] = j < lim ? sv[j] : -INFINITY;
+                    }
+                    float mx[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) mx[j] = sv[j];
+#pragma unroll
+                    for (int j = 4; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], sv[j]);
+                    float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                    rmax = fmaxf(rmax, __shfl_xor_sync(kFull, rmax, 16)) * p.scale_log2;
+                    // Exponent base: the row max on a chunk's first item; later,
+                    // only when the max passes the base by more than 2^8.
+                    const bool first = item == i0;
+                    const bool need = !first && rmax > m_used + kRescaleThreshold;
+                    const float m_new = (first || need) ? rmax : m_used;
+                    const float f = need ? exp2_approx(m_used - m_new) : 1.f;
+                    uint32_t pk[16];
+                    float rs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float p0 = exp2_approx(fmaf(sv[2 * j], p.scale_log2, -m_new));
+                        const float p1 = exp2_approx(fmaf(sv[2 * j + 1], p.scale_log2, -m_new));
+                        rs[j & 3] += p0 + p1;
+                        pk[j] = pack_bf16(p0, p1);
+                    }
+                    lsum = (first ? 0.f : lsum * f) + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+                    m_used = m_new;
+                    // P row of this lane: its half of the keys, zeros elsewhere.
+                    uint32_t prow[32];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        prow[j] = half ? 0u : pk[j];
+                        prow[16 + j] = half ? pk[j] : 0u;
+                    }
+                    tmem_st32(tmem + lane_off + kColP + 32u * b, prow);
+                    tmem_wait_st();
+                    // The previous item's PV must be complete before O may be
+                    // touched; confirming it at every item also keeps this
+                    // thread within one phase of o_done.
+                    if (it > 0) {
+                        mbar_wait(bar_odone, static_cast<uint32_t>((it - 1) & 1), abort_flag, p.status);
+                        fence_after();
+                    }
+                    if (__any_sync(kFull, need)) {
+                        uint32_t orr[64];
+                        tmem_ld64(tmem + lane_off + kColO, orr);
+                        uint32_t part[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) part[j] = __float_as_uint(__uint_as_float(orr[j]) * f);
+                        tmem_st32(tmem + lane_off + kColO, part);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) part[j] = __float_as_uint(__uint_as_float(orr[32 + j]) * f);
+                        tmem_st32(tmem + lane_off + kColO + 32u, part);
+                        tmem_wait_st();
+                    }
+                    if (is_page && valid < kP) {
+                        // Stale pool slots past the context may hold
+                        // non-finite values: zero them before P.V reads them.
+                        uint4 *vt = reinterpret_cast<uint4 *>(smem + kOffStages + s * kStageBytes + kTileBytes);
+                        for (int e = t; e < (kP - valid) * 8; e += kRowThreads) vt[valid * 8 + e] = make_uint4(0, 0, 0, 0);
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    }
+                    fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_pfull + 8 * b);
+                    ++it;
+                    if (is_page) ++kr;
+                }
+                // ---- chunk partial: add the two lanes' halves, write O, m, l.
+                mbar_wait(bar_odone, static_cast<uint32_t>((it - 1) & 1), abort_flag, p.status);
+                fence_after();
+                uint32_t orr[64];
+                tmem_ld64(tmem + lane_off + kColO, orr);
+                const float ltot = lsum + __shfl_xor_sync(kFull, lsum, 16);
+                float outv[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    // lane half 0 keeps dims 0..31, half 1 dims 32..63.
+                    const float give = __uint_as_float(half ? orr[j] : orr[32 + j]);
+                    const float keep = __uint_as_float(half ? orr[32 + j] : orr[j]);
+                    outv[j] = keep + __shfl_xor_sync(kFull, give, 16);
+                }
+                if (active) {
+                    const long long slot = static_cast<long long>(pl->cstart[u]) + jc;
+                    float4 *dst = reinterpret_cast<float4 *>(p.ws_o + slot * kPartialFloats + rho * kD + 32 * half);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        dst[j] = make_float4(outv[4 * j], outv[4 * j + 1], outv[4 * j + 2], outv[4 * j + 3]);
+                    if (half == 0) p.ws_ml[slot * kRows + rho] = make_float2(m_used, ltot);
+                }
+                fence_before();
+            }
+        }
+    }
+
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == kMmaWarp)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------- combine --
 //
 // One CTA per (unit, 2 query rows), 256 threads: thread = (row, 8 dims,
@@ -877,6 +1438,52 @@ __global__ void __launch_bounds__(256) k3da_combine_kernel(const __grid_constant
 
 // ------------------------------------------------------------------ host --
 
+// The split pass that runs: the tcgen05 one unless built with
+// K3DA_USE_TCGEN05=0 (the mma.sync one).
+#ifndef K3DA_USE_TCGEN05
+#define K3DA_USE_TCGEN05 1
+#endif
+#if K3DA_USE_TCGEN05
+constexpr int kSplitThreads = tc::kThreads;
+constexpr int kSplitSmem = tc::kSmemBytes;
+#define kSplitLaunch k3da_tc_kernel
+#else
+constexpr int kSplitThreads = kThreads;
+constexpr int kSplitSmem = kSmemBytes;
+#define kSplitLaunch k3da_split_kernel
+#endif
+const void *const kSplitKernel[2] = {reinterpret_cast<const void *>(&kSplitLaunch<false>),
+                                     reinterpret_cast<const void *>(&kSplitLaunch<true>)};
+
+// CTAs of `kernel` that fit on one SM: registers (per-warp allocation in
+// units of 256), shared memory (with the per-block reservation), threads,
+// and, for the tcgen05 pass, tensor-memory columns (512 per SM).  Computed
+// from the kernel's attributes because the runtime's occupancy query counts
+// the tcgen05 pass as one CTA per SM.
+int occupancy_of(const void *kernel, int threads, int dyn_smem, int dev, int *occ) {
+    cudaFuncAttributes fa;
+    int smem_sm = 0, smem_rsv = 0, regs_sm = 0, thr_sm = 0, blk_sm = 0;
+    if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&blk_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev) != cudaSuccess)
+        return K3DA_ECUDA;
+    const int warps = (threads + 31) / 32;
+    const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+    int n = blk_sm;
+    if (regs_warp > 0) n = n < regs_sm / (regs_warp * warps) ? n : regs_sm / (regs_warp * warps);
+    const int smem_block = static_cast<int>(fa.sharedSizeBytes) + dyn_smem + smem_rsv;
+    n = n < smem_sm / smem_block ? n : smem_sm / smem_block;
+    n = n < thr_sm / (warps * 32) ? n : thr_sm / (warps * 32);
+#if K3DA_USE_TCGEN05
+    n = n < static_cast<int>(512 / tc::kTmemCols) ? n : static_cast<int>(512 / tc::kTmemCols);
+#endif
+    *occ = n;
+    return K3DA_OK;
+}
+
 struct DeviceConfig {
     bool ready;
     int sms;
@@ -899,16 +1506,18 @@ int configure_device(int dev, DeviceConfig *cfg) {
         int rc = K3DA_OK;
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) rc = K3DA_ECUDA;
-        const void *kernels[2] = {reinterpret_cast<const void *>(&k3da_split_kernel<false>),
-                                  reinterpret_cast<const void *>(&k3da_split_kernel<true>)};
+        const void *kernels[2] = {kSplitKernel[0], kSplitKernel[1]};
         int occ[2] = {0, 0};
         for (int v = 0; v < 2 && rc == K3DA_OK; ++v) {
-            if (cudaFuncSetAttribute(kernels[v], cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-                cudaSuccess)
+            // Ask for the largest shared-memory carveout, then size the grid
+            // from the occupancy it allows.
+            if (cudaFuncSetAttribute(kernels[v], cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem) !=
+                    cudaSuccess ||
+                cudaFuncSetAttribute(kernels[v], cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared) != cudaSuccess)
                 rc = K3DA_ECUDA;
-            else if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[v], kernels[v], kThreads, kSmemBytes) !=
-                     cudaSuccess)
-                rc = K3DA_ECUDA;
+            else
+                rc = occupancy_of(kernels[v], kSplitThreads, kSplitSmem, dev, &occ[v]);
         }
         if (rc == K3DA_OK && g_encode == nullptr) {
             cudaDriverEntryPointQueryResult q;
@@ -1022,9 +1631,9 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (qknorm)
-        k3da_split_kernel<true><<<prm.grid, kThreads, kSmemBytes, st>>>(map, prm);
+        kSplitLaunch<true><<<prm.grid, kSplitThreads, kSplitSmem, st>>>(map, prm);
     else
-        k3da_split_kernel<false><<<prm.grid, kThreads, kSmemBytes, st>>>(map, prm);
+        kSplitLaunch<false><<<prm.grid, kSplitThreads, kSplitSmem, st>>>(map, prm);
     if (cudaGetLastError() != cudaSuccess) return K3DA_ECUDA;
     if (g_phase_event && cudaEventRecord(g_phase_event, st) != cudaSuccess) return K3DA_ECUDA;
     // The combine is a programmatic dependent of the split pass, so its
@@ -1074,6 +1683,14 @@ int k3da_attn_qknorm(void *out, const void *qkv, const void *kv_pool, int64_t nu
     return launch(out, qkv, kv_pool, num_pages, page_table, page_stride, ctx_lens, num_requests, block_len,
                   num_q_heads, num_kv_heads, head_dim, softmax_scale, true, positions, pos_dtype, q_norm_w,
                   k_norm_w, eps, rope_base, workspace, workspace_bytes, status, stream);
+}
+
+int k3da_split_grid(int device) {
+    int dev = device;
+    if (dev < 0 && cudaGetDevice(&dev) != cudaSuccess) return 0;
+    DeviceConfig cfg;
+    if (configure_device(dev, &cfg) != K3DA_OK) return 0;
+    return cfg.sms * cfg.occupancy[1];
 }
 
 int k3da_set_phase_event(void *event) {

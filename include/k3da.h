@@ -142,6 +142,41 @@ int k3da_attn_qknorm(void *out, const void *qkv, const void *kv_pool, int64_t nu
 int k3da_set_phase_event(void *event);
 
 /*
+ * k3da_attn_qknorm_noalloc -- k3da_attn_qknorm for callers that cannot
+ * allocate device memory: code that runs where cudaMalloc is unavailable or
+ * forbidden (a host callback, a real-time path that must not allocate, a
+ * plugin whose host framework owns every device allocation) or that has no
+ * way to keep a workspace buffer between calls.  Not an operation of the ops this library implements
+ * (the paper has no counterpart): the same computation as k3da_attn_qknorm,
+ * with the scratch taken from a fixed array of k3da_noalloc_scratch_bytes()
+ * (8 MiB) that the library keeps in the memory of every GPU it is loaded on,
+ * for the life of the process.  Arguments are those of k3da_attn_qknorm
+ * without workspace / workspace_bytes; the caller still passes every input
+ * and output.
+ *
+ * - Sizes whose workspace (k3da_workspace_bytes) exceeds the array are
+ *   refused with K3DA_EWORKSPACE: page_stride <= 511 always fits.
+ * - Nothing is allocated or freed, by the library or by any routine it
+ *   calls.
+ * - The first call on a device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ * - All calls on a device share the one array.  Its contents on entry do not
+ *   matter (every value read is first written by the same call), but two
+ *   calls that overlap on the GPU (different streams, no ordering) race on
+ *   it: order them, or use k3da_attn_qknorm with separate workspaces.
+ */
+int k3da_attn_qknorm_noalloc(void *out, const void *qkv, const void *kv_pool, int64_t num_pages,
+                             const int32_t *page_table, int page_stride, const int32_t *ctx_lens,
+                             int num_requests, int block_len, int num_q_heads,
+                             int num_kv_heads, int head_dim, float softmax_scale,
+                             const void *positions, int pos_dtype, const void *q_norm_w,
+                             const void *k_norm_w, float eps, float rope_base, int32_t *status,
+                             void *stream);
+
+/* Bytes of the fixed scratch array k3da_attn_qknorm_noalloc uses. */
+size_t k3da_noalloc_scratch_bytes(void);
+
+/*
  * CTAs the split pass launches on `device` (-1 = current): SM count times
  * the CTAs per SM its resources allow.  Configures the device like a first
  * call does.  Returns 0 when the device cannot be configured.

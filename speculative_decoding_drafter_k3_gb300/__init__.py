@@ -35,8 +35,9 @@ _lib = None
 OK, EINVAL, EUNSUPPORTED, ECUDA, EWORKSPACE = 0, -1, -2, -3, -4
 STATUS_BAD_LENGTH, STATUS_BAD_PAGE, STATUS_TIMEOUT = 1, 2, 4
 POS_I32, POS_I64 = 0, 1
-EXPORTED = ["k3da_workspace_bytes", "k3da_attn", "k3da_attn_qknorm", "k3da_split_grid",
-            "k3da_set_phase_event", "k3da_error_string", "k3da_version"]
+EXPORTED = ["k3da_workspace_bytes", "k3da_attn", "k3da_attn_qknorm", "k3da_attn_qknorm_noalloc",
+            "k3da_noalloc_scratch_bytes", "k3da_split_grid", "k3da_set_phase_event",
+            "k3da_error_string", "k3da_version"]
 
 
 class K3daError(ValueError):
@@ -69,6 +70,10 @@ def load_library():
         lib.k3da_attn_qknorm.restype = c_int
         lib.k3da_error_string.argtypes = [c_int]
         lib.k3da_error_string.restype = ctypes.c_char_p
+        lib.k3da_attn_qknorm_noalloc.argtypes = common + [vp, c_int, vp, vp, c_f, c_f, vp, vp]
+        lib.k3da_attn_qknorm_noalloc.restype = c_int
+        lib.k3da_noalloc_scratch_bytes.argtypes = []
+        lib.k3da_noalloc_scratch_bytes.restype = c_sz
         lib.k3da_split_grid.argtypes = [c_int]
         lib.k3da_split_grid.restype = c_int
         lib.k3da_set_phase_event.argtypes = [vp]
@@ -210,3 +215,25 @@ def set_phase_event(event):
 def split_grid(device: int = -1) -> int:
     """CTAs the split pass launches on ``device`` (SMs x CTAs per SM)."""
     return int(load_library().k3da_split_grid(device))
+
+
+def k3da_attn_qknorm_noalloc(out, qkv, kv_pool, page_table, ctx_lens, positions, q_norm_w, k_norm_w, *,
+                             block_len: int, num_q_heads: int, num_kv_heads: int,
+                             softmax_scale: float = 0.125, eps: float = 1e-5,
+                             rope_base: float = 10000.0, status=None, stream=None):
+    """k3da_attn_qknorm without a workspace argument, for callers that cannot
+    allocate: the library's fixed per-GPU scratch array is used instead
+    (C: k3da_attn_qknorm_noalloc; calls that overlap on the GPU race on it)."""
+    lib = load_library()
+    R, num_pages, S, D = _shape_args(out, qkv, kv_pool, page_table, ctx_lens, block_len,
+                                     num_q_heads, num_kv_heads)
+    if positions.dtype not in (torch.int32, torch.int64) or positions.numel() != R * block_len:
+        raise K3daError("positions must be [T] int32 or int64")
+    pos_code = POS_I64 if positions.dtype == torch.int64 else POS_I32
+    rc = lib.k3da_attn_qknorm_noalloc(_ptr(out), _ptr(qkv), _ptr(kv_pool), num_pages, _ptr(page_table),
+                                      S, _ptr(ctx_lens), R, block_len, num_q_heads, num_kv_heads, D,
+                                      float(softmax_scale), _ptr(positions), pos_code, _ptr(q_norm_w),
+                                      _ptr(k_norm_w), float(eps), float(rope_base), _ptr(status),
+                                      _stream(stream))
+    _check(rc, "k3da_attn_qknorm_noalloc")
+    return out

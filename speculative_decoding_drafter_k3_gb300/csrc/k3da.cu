@@ -1560,6 +1560,32 @@ size_t workspace_for(int R, int Hkv, int page_stride) {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Scratch of k3da_attn_qknorm_noalloc: a fixed array in device memory that
+// exists on every GPU this library is loaded on, for callers that cannot
+// allocate.  8 MiB covers every shape with page_stride <= 511.
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch on `dev`, looked up once per device with
+// that device current (the host-side symbol is only a stand-in).
+int static_scratch_address(int dev, void **out) {
+    static void *addr[128] = {nullptr};
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (dev < 0 || dev >= 128) return K3DA_EINVAL;
+    if (addr[dev] == nullptr) {
+        int prev = -1;
+        if (cudaGetDevice(&prev) != cudaSuccess) return K3DA_ECUDA;
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) return K3DA_ECUDA;
+        void *ptr = nullptr;
+        const cudaError_t rc = cudaGetSymbolAddress(&ptr, g_static_scratch);
+        if (prev != dev) cudaSetDevice(prev);
+        if (rc != cudaSuccess || ptr == nullptr) return K3DA_ECUDA;
+        addr[dev] = ptr;
+    }
+    *out = addr[dev];
+    return K3DA_OK;
+}
+
 int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, const int32_t *page_table,
            int page_stride, const int32_t *ctx_lens, int R, int B, int Hq, int Hkv, int head_dim,
            float softmax_scale, bool qknorm, const void *positions, int pos_dtype, const void *q_norm_w,
@@ -1684,6 +1710,25 @@ int k3da_attn_qknorm(void *out, const void *qkv, const void *kv_pool, int64_t nu
                   num_q_heads, num_kv_heads, head_dim, softmax_scale, true, positions, pos_dtype, q_norm_w,
                   k_norm_w, eps, rope_base, workspace, workspace_bytes, status, stream);
 }
+
+int k3da_attn_qknorm_noalloc(void *out, const void *qkv, const void *kv_pool, int64_t num_pages,
+                             const int32_t *page_table, int page_stride, const int32_t *ctx_lens,
+                             int num_requests, int block_len, int num_q_heads, int num_kv_heads, int head_dim,
+                             float softmax_scale, const void *positions, int pos_dtype, const void *q_norm_w,
+                             const void *k_norm_w, float eps, float rope_base, int32_t *status, void *stream) {
+    if (num_requests < 1 || num_requests > kMaxR || num_kv_heads < 1 || page_stride < 1) return K3DA_EINVAL;
+    if (workspace_for(num_requests, num_kv_heads, page_stride) > kStaticScratchBytes) return K3DA_EWORKSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return K3DA_ECUDA;
+    void *scratch = nullptr;
+    const int rc = static_scratch_address(dev, &scratch);
+    if (rc != K3DA_OK) return rc;
+    return launch(out, qkv, kv_pool, num_pages, page_table, page_stride, ctx_lens, num_requests, block_len,
+                  num_q_heads, num_kv_heads, head_dim, softmax_scale, true, positions, pos_dtype, q_norm_w,
+                  k_norm_w, eps, rope_base, scratch, kStaticScratchBytes, status, stream);
+}
+
+size_t k3da_noalloc_scratch_bytes(void) { return kStaticScratchBytes; }
 
 int k3da_split_grid(int device) {
     int dev = device;

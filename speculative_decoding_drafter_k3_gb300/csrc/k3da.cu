@@ -845,7 +845,8 @@ constexpr int kOffBlkK = kOffQ + 128 * 128;          // 64 rows x 128 B
 constexpr int kOffBlkV = kOffBlkK + 64 * 128;        // 64 rows x 128 B
 constexpr int kOffRaw = kOffBlkV + 64 * 128;         // raw q [8][6][64], k [8][64], v [8][64]
 constexpr int kOffTrig = kOffRaw + kMaxB * (kG + 2) * kD * 2;  // [8][32] float2
-constexpr int kOffPlan = kOffTrig + kMaxB * 32 * 8;
+constexpr int kOffNormW = kOffTrig + kMaxB * 32 * 8;  // q and k norm weights, [2][64] float
+constexpr int kOffPlan = kOffNormW + 2 * kD * 4;
 constexpr int kNumBars = 2 * kStages + 7;  // full, empty, s_full[2], p_full[2], o_done, q_ready, done
 constexpr int kOffBar = kOffPlan + 1536;
 constexpr int kOffTaddr = kOffBar + kNumBars * 8;
@@ -935,6 +936,7 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
     constexpr auto kOffBlkV = tc::kOffBlkV;
     constexpr auto kOffRaw = tc::kOffRaw;
     constexpr auto kOffTrig = tc::kOffTrig;
+    constexpr auto kOffNormW = tc::kOffNormW;
     constexpr auto kOffPlan = tc::kOffPlan;
     constexpr auto kNumBars = tc::kNumBars;
     constexpr auto kOffBar = tc::kOffBar;
@@ -1144,13 +1146,8 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
         uint8_t *raw_v = raw_k + kMaxB * kD * 2;
         float2 *trig = reinterpret_cast<float2 *>(smem + kOffTrig);
         const long long row_w = static_cast<long long>(p.Hq + 2 * p.Hkv) * kD;
-        float wq_lo = 1.f, wq_hi = 1.f, wk_lo = 1.f, wk_hi = 1.f;
-        if (QKNORM) {
-            wq_lo = __bfloat162float(p.q_w[lane]);
-            wq_hi = __bfloat162float(p.q_w[lane + 32]);
-            wk_lo = __bfloat162float(p.k_w[lane]);
-            wk_hi = __bfloat162float(p.k_w[lane + 32]);
-        }
+        float *normw = reinterpret_cast<float *>(smem + kOffNormW);  // [0..63] q, [64..127] k
+        if (QKNORM) normw[t] = __bfloat162float(t < kD ? p.q_w[t] : p.k_w[t - kD]);
         long long it = 0, kr = 0;
         for (int rn = 0; rn < nrun; ++rn) {
             const int u = pl->run_u[rn];
@@ -1204,28 +1201,95 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
             }
             cp_async_wait_all();
             named_bar_sync(1, kRowThreads);
-            const int prep_rows = with_block ? kRows + 2 * kMaxB : kRows;
-            for (int pr = warp; pr < prep_rows; pr += kRowWarps) {
-                if (pr < kRows) {
-                    if (pr < rows) {
-                        const int g = pr / p.B, ti = pr - g * p.B;
-                        const int idx = (ti * kG + g) * kD;
-                        const int trow = (pr / kRowsPerQuarter) * 32 + pr % kRowsPerQuarter;
-                        prep_row<QKNORM>(qtile, trow, bf16_at(raw_q, idx + lane), bf16_at(raw_q, idx + lane + 32),
-                                         wq_lo, wq_hi, p.eps, QKNORM ? trig[ti * 32 + lane] : make_float2(1.f, 0.f),
-                                         lane, trow + 16);
+            // Two threads per row: thread t takes row t/2 and the 16 RoPE
+            // pairs (j, j+32) with j in [16*(t&1), 16*(t&1)+16).  Rows 0..47
+            // are query rows (g*B + i), 48..55 block keys, 56..63 block values.
+            {
+                const int rix = t >> 1, hp = t & 1;
+                const uint8_t *src = nullptr;
+                uint8_t *dst = nullptr;
+                int drow = 0, drow2 = -1, ti = 0;
+                bool norm = false;
+                const float *w = normw;
+                if (rix < kRows) {
+                    if (rix < rows) {
+                        const int g = rix / p.B;
+                        ti = rix - g * p.B;
+                        src = raw_q + (ti * kG + g) * 128;
+                        dst = qtile;
+                        drow = (rix / kRowsPerQuarter) * 32 + rix % kRowsPerQuarter;
+                        drow2 = drow + 16;
+                        norm = QKNORM;
                     }
-                } else if (pr < kRows + kMaxB) {
-                    const int j = pr - kRows;
-                    if (j < p.B)
-                        prep_row<QKNORM>(bk, j, bf16_at(raw_k, j * kD + lane), bf16_at(raw_k, j * kD + lane + 32),
-                                         wk_lo, wk_hi, p.eps, QKNORM ? trig[j * 32 + lane] : make_float2(1.f, 0.f),
-                                         lane);
+                } else if (rix < kRows + kMaxB) {
+                    const int j = rix - kRows;
+                    if (with_block && j < p.B) {
+                        ti = j;
+                        src = raw_k + j * 128;
+                        dst = bk;
+                        drow = j;
+                        norm = QKNORM;
+                        w = normw + kD;
+                    }
                 } else {
-                    const int j = pr - kRows - kMaxB;
-                    if (j < p.B)
-                        prep_row<false>(bv, j, bf16_at(raw_v, j * kD + lane), bf16_at(raw_v, j * kD + lane + 32),
-                                        1.f, 1.f, 0.f, make_float2(1.f, 0.f), lane);
+                    const int j = rix - kRows - kMaxB;
+                    if (with_block && j < p.B) {
+                        src = raw_v + j * 128;
+                        dst = bv;
+                        drow = j;
+                    }
+                }
+                float lo[16], hi[16];
+                if (src != nullptr) {
+                    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+                    const uint4 a0 = s4[2 * hp], a1 = s4[2 * hp + 1], b0 = s4[4 + 2 * hp], b1 = s4[4 + 2 * hp + 1];
+                    const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                    const uint32_t bv2[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        lo[2 * e] = __uint_as_float(av[e] << 16);
+                        lo[2 * e + 1] = __uint_as_float(av[e] & 0xffff0000u);
+                        hi[2 * e] = __uint_as_float(bv2[e] << 16);
+                        hi[2 * e + 1] = __uint_as_float(bv2[e] & 0xffff0000u);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) lo[e] = hi[e] = 0.f;
+                }
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) ss = fmaf(lo[e], lo[e], fmaf(hi[e], hi[e], ss));
+                ss += __shfl_xor_sync(kFull, ss, 1);
+                if (norm) {
+                    const float inv = rsqrtf(ss * (1.0f / kD) + p.eps);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int jp = 16 * hp + e;
+                        const float n_lo = lo[e] * inv * w[jp];
+                        const float n_hi = hi[e] * inv * w[jp + 32];
+                        const float2 cs = trig[ti * 32 + jp];
+                        lo[e] = n_lo * cs.x - n_hi * cs.y;
+                        hi[e] = n_hi * cs.x + n_lo * cs.y;
+                    }
+                }
+                if (dst != nullptr) {
+                    uint4 o[4];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        o[c] = make_uint4(pack_bf16(lo[8 * c], lo[8 * c + 1]), pack_bf16(lo[8 * c + 2], lo[8 * c + 3]),
+                                          pack_bf16(lo[8 * c + 4], lo[8 * c + 5]), pack_bf16(lo[8 * c + 6], lo[8 * c + 7]));
+                        o[2 + c] = make_uint4(pack_bf16(hi[8 * c], hi[8 * c + 1]), pack_bf16(hi[8 * c + 2], hi[8 * c + 3]),
+                                              pack_bf16(hi[8 * c + 4], hi[8 * c + 5]), pack_bf16(hi[8 * c + 6], hi[8 * c + 7]));
+                    }
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        *reinterpret_cast<uint4 *>(dst + swz(drow, 2 * hp + c)) = o[c];
+                        *reinterpret_cast<uint4 *>(dst + swz(drow, 4 + 2 * hp + c)) = o[2 + c];
+                        if (drow2 >= 0) {
+                            *reinterpret_cast<uint4 *>(dst + swz(drow2, 2 * hp + c)) = o[c];
+                            *reinterpret_cast<uint4 *>(dst + swz(drow2, 4 + 2 * hp + c)) = o[2 + c];
+                        }
+                    }
                 }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

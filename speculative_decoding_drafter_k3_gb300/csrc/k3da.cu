@@ -1148,6 +1148,33 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
         const long long row_w = static_cast<long long>(p.Hq + 2 * p.Hkv) * kD;
         float *normw = reinterpret_cast<float *>(smem + kOffNormW);  // [0..63] q, [64..127] k
         if (QKNORM) normw[t] = __bfloat162float(t < kD ? p.q_w[t] : p.k_w[t - kD]);
+        // A chunk's partial is written while the next chunk's first item is in
+        // flight (its P.V, the last O reader, was confirmed just before), so
+        // the wait for the chunk's last P.V hides behind that item's softmax.
+        bool epi_pending = false;
+        long long epi_slot = 0;
+        float epi_m = 0.f, epi_l = 0.f;
+        auto write_partial = [&]() {
+            uint32_t orr[64];
+            tmem_ld64(tmem + lane_off + kColO, orr);
+            const float ltot = epi_l + __shfl_xor_sync(kFull, epi_l, 16);
+            float outv[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                // lane half 0 keeps dims 0..31, half 1 dims 32..63.
+                const float give = __uint_as_float(half ? orr[j] : orr[32 + j]);
+                const float keep = __uint_as_float(half ? orr[32 + j] : orr[j]);
+                outv[j] = keep + __shfl_xor_sync(kFull, give, 16);
+            }
+            if (active) {
+                float4 *dst = reinterpret_cast<float4 *>(p.ws_o + epi_slot * kPartialFloats + rho * kD + 32 * half);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    dst[j] = make_float4(outv[4 * j], outv[4 * j + 1], outv[4 * j + 2], outv[4 * j + 3]);
+                if (half == 0) p.ws_ml[epi_slot * kRows + rho] = make_float2(epi_m, ltot);
+            }
+            epi_pending = false;
+        };
         long long it = 0, kr = 0;
         for (int rn = 0; rn < nrun; ++rn) {
             const int u = pl->run_u[rn];
@@ -1362,6 +1389,7 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
                         mbar_wait(bar_odone, static_cast<uint32_t>((it - 1) & 1), abort_flag, p.status);
                         fence_after();
                     }
+                    if (epi_pending) write_partial();  // before this item's P.V overwrites O
                     if (__any_sync(kFull, need)) {
                         uint32_t orr[64];
                         tmem_ld64(tmem + lane_off + kColO, orr);
@@ -1387,31 +1415,19 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
                     ++it;
                     if (is_page) ++kr;
                 }
-                // ---- chunk partial: add the two lanes' halves, write O, m, l.
-                mbar_wait(bar_odone, static_cast<uint32_t>((it - 1) & 1), abort_flag, p.status);
-                fence_after();
-                uint32_t orr[64];
-                tmem_ld64(tmem + lane_off + kColO, orr);
-                const float ltot = lsum + __shfl_xor_sync(kFull, lsum, 16);
-                float outv[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    // lane half 0 keeps dims 0..31, half 1 dims 32..63.
-                    const float give = __uint_as_float(half ? orr[j] : orr[32 + j]);
-                    const float keep = __uint_as_float(half ? orr[32 + j] : orr[j]);
-                    outv[j] = keep + __shfl_xor_sync(kFull, give, 16);
-                }
-                if (active) {
-                    const long long slot = static_cast<long long>(pl->cstart[u]) + jc;
-                    float4 *dst = reinterpret_cast<float4 *>(p.ws_o + slot * kPartialFloats + rho * kD + 32 * half);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        dst[j] = make_float4(outv[4 * j], outv[4 * j + 1], outv[4 * j + 2], outv[4 * j + 3]);
-                    if (half == 0) p.ws_ml[slot * kRows + rho] = make_float2(m_used, ltot);
-                }
-                fence_before();
+                // ---- chunk partial: written during the next item (or below).
+                epi_pending = true;
+                epi_slot = static_cast<long long>(pl->cstart[u]) + jc;
+                epi_m = m_used;
+                epi_l = lsum;
             }
         }
+        if (epi_pending) {
+            mbar_wait(bar_odone, static_cast<uint32_t>((it - 1) & 1), abort_flag, p.status);
+            fence_after();
+            write_partial();
+        }
+        fence_before();
     }
 
     fence_before();
@@ -1426,13 +1442,15 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
 //
 // One CTA per (unit, 2 query rows), 256 threads: thread = (row, 8 dims,
 // chunk lane sg of 16), the 16 chunk lanes of one (row, dims) sitting in one
-// half-warp.  Lane sg folds the unit's chunk partials sg, sg+16, ... online;
-// the lanes then merge by a fixed butterfly of shuffles, so the result
-// depends on nothing but the unit's own chunks.  Launched as a programmatic
-// dependent of the split pass: the prologue overlaps its tail and
-// griddepcontrol.wait orders the partial reads after it.
+// half-warp.  Lane sg folds the unit's chunk partials sg, sg+16, ... online,
+// loading up to kCombineFold of them at once; the lanes then merge by a
+// fixed butterfly of shuffles, so the result depends on nothing but the
+// unit's own chunks.  Launched as a programmatic dependent of the split
+// pass: the prologue overlaps its tail and griddepcontrol.wait orders the
+// partial reads after it.
 constexpr int kCombineRows = 2;
 constexpr int kCombineLanes = 16;
+constexpr int kCombineFold = 4;
 
 __global__ void __launch_bounds__(256) k3da_combine_kernel(const __grid_constant__ Params p) {
     __shared__ Plan pl;
@@ -1449,24 +1467,40 @@ __global__ void __launch_bounds__(256) k3da_combine_kernel(const __grid_constant
     float m = -INFINITY, l = 0.f;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (row < rows) {
-#pragma unroll 4
-        for (int j = sg; j < nch; j += kCombineLanes) {
-            const long long slot = slot0 + j;
-            const float2 ml = p.ws_ml[slot * kRows + row];
-            const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + slot * kPartialFloats + row * kD + dc * 8);
-            const float4 v0 = src[0], v1 = src[1];
-            const float mm = fmaxf(m, ml.x);
-            const float fo = exp2_approx(m - mm), fn = exp2_approx(ml.x - mm);
-            m = mm;
-            l = l * fo + ml.y * fn;
-            acc[0] = acc[0] * fo + v0.x * fn;
-            acc[1] = acc[1] * fo + v0.y * fn;
-            acc[2] = acc[2] * fo + v0.z * fn;
-            acc[3] = acc[3] * fo + v0.w * fn;
-            acc[4] = acc[4] * fo + v1.x * fn;
-            acc[5] = acc[5] * fo + v1.y * fn;
-            acc[6] = acc[6] * fo + v1.z * fn;
-            acc[7] = acc[7] * fo + v1.w * fn;
+        for (int base = 0; base < nch; base += kCombineLanes * kCombineFold) {
+            float2 ml[kCombineFold];
+            float4 v0[kCombineFold], v1[kCombineFold];
+#pragma unroll
+            for (int f = 0; f < kCombineFold; ++f) {
+                const int j = base + sg + f * kCombineLanes;
+                if (j < nch) {
+                    const long long slot = slot0 + j;
+                    ml[f] = p.ws_ml[slot * kRows + row];
+                    const float4 *src =
+                        reinterpret_cast<const float4 *>(p.ws_o + slot * kPartialFloats + row * kD + dc * 8);
+                    v0[f] = src[0];
+                    v1[f] = src[1];
+                } else {
+                    ml[f] = make_float2(-INFINITY, 0.f);
+                    v0[f] = v1[f] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int f = 0; f < kCombineFold; ++f) {
+                const float mm = fmaxf(m, ml[f].x);
+                if (mm == -INFINITY) continue;  // nothing folded yet and no chunk here
+                const float fo = exp2_approx(m - mm), fn = exp2_approx(ml[f].x - mm);
+                m = mm;
+                l = l * fo + ml[f].y * fn;
+                acc[0] = acc[0] * fo + v0[f].x * fn;
+                acc[1] = acc[1] * fo + v0[f].y * fn;
+                acc[2] = acc[2] * fo + v0[f].z * fn;
+                acc[3] = acc[3] * fo + v0[f].w * fn;
+                acc[4] = acc[4] * fo + v1[f].x * fn;
+                acc[5] = acc[5] * fo + v1[f].y * fn;
+                acc[6] = acc[6] * fo + v1[f].z * fn;
+                acc[7] = acc[7] * fo + v1[f].w * fn;
+            }
         }
     }
 #pragma unroll
@@ -1499,8 +1533,6 @@ __global__ void __launch_bounds__(256) k3da_combine_kernel(const __grid_constant
                                    static_cast<long long>(h * kG + g) * kD + dc * 8) = packed;
     }
 }
-
-// ------------------------------------------------------------------ host --
 
 // The split pass that runs: the tcgen05 one unless built with
 // K3DA_USE_TCGEN05=0 (the mma.sync one).

@@ -329,7 +329,7 @@ def run_ours(args, world, rank):
 
     # Roofline: the split pass alone, bracketed by an event the library
     # records between its two kernels.
-    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     for e in pev:
         e[1].record()  # torch creates its events lazily: create the one the library records
     torch.cuda.synchronize()
@@ -338,9 +338,11 @@ def run_ours(args, world, rank):
         pev[i][0].record()
         k3da.set_phase_event(pev[i][1])
         call()
+        pev[i][2].record()
     torch.cuda.synchronize()
     k3da.set_phase_event(None)
     split_ms = [e[0].elapsed_time(e[1]) for e in pev]
+    combine_ms = [e[1].elapsed_time(e[2]) for e in pev]  # combine after the event: no launch overlap
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     value = total_ms * 1e3 / (K * world)
 
@@ -384,6 +386,7 @@ def run_ours(args, world, rank):
                 "kernel": "k3da_split_kernel (split pass; combine excluded)",
                 "algorithmic_bytes_per_launch": split_bytes, "launch_us": split_us,
                 "peak_source": peak_src,
+                "combine_us_unoverlapped": statistics.mean(combine_ms) * 1e3,
                 "whole_call_gbs": case.algorithmic_bytes() / (value * 1e-6) / 1e9}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,

@@ -103,6 +103,7 @@ struct Params {
     const void *positions;
     const __nv_bfloat16 *q_w;
     const __nv_bfloat16 *k_w;
+    int *ws_units;      // [2][32]: first chunk slot and chunk count of each unit
     float *ws_o;        // [slots][48][64]
     float2 *ws_ml;      // [slots][48]  (m in log2 units, l)
     int32_t *status;
@@ -531,6 +532,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     __syncthreads();
     const int nrun = pl->nrun;
+    if (blockIdx.x == 0 && threadIdx.x < p.R * p.Hkv) {
+        p.ws_units[threadIdx.x] = pl->cstart[threadIdx.x];
+        p.ws_units[kMaxUnits + threadIdx.x] = pl->nch[threadIdx.x];
+    }
     if (nrun == 0) {
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         return;
@@ -999,6 +1004,12 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
     fence_after();
     const uint32_t tmem = *taddr_slot;
     const int nrun = pl->nrun;
+    if (blockIdx.x == 0 && threadIdx.x < p.R * p.Hkv) {
+        // The combine reads each unit's chunk slots from here instead of
+        // rebuilding the plan.
+        p.ws_units[threadIdx.x] = pl->cstart[threadIdx.x];
+        p.ws_units[kMaxUnits + threadIdx.x] = pl->nch[threadIdx.x];
+    }
 
     if (warp == kProducerWarp && nrun > 0) {
         // ------------------------------------------------ producer warp --
@@ -1440,30 +1451,28 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
 
 // --------------------------------------------------------------- combine --
 //
-// One CTA per (unit, 2 query rows), 256 threads: thread = (row, 8 dims,
-// chunk lane sg of 16), the 16 chunk lanes of one (row, dims) sitting in one
-// half-warp.  Lane sg folds the unit's chunk partials sg, sg+16, ... online,
-// loading up to kCombineFold of them at once; the lanes then merge by a
-// fixed butterfly of shuffles, so the result depends on nothing but the
-// unit's own chunks.  Launched as a programmatic dependent of the split
-// pass: the prologue overlaps its tail and griddepcontrol.wait orders the
-// partial reads after it.
+// One CTA per (unit, 2 query rows), 128 threads: thread = (row, 8 dims,
+// chunk lane sg of 8), the 8 chunk lanes of one (row, dims) adjacent in a
+// warp.  Lane sg folds the unit's chunk partials sg, sg+8, ... online,
+// loading kCombineFold of them at once; the lanes then merge by a fixed
+// butterfly of shuffles, so the result depends on nothing but the unit's
+// own chunks.  The unit's chunk slots come from the table the split pass
+// writes.  Launched as a programmatic dependent of the split pass:
+// griddepcontrol.wait orders every workspace read after it.
 constexpr int kCombineRows = 2;
-constexpr int kCombineLanes = 16;
+constexpr int kCombineLanes = 8;
 constexpr int kCombineFold = 4;
 
-__global__ void __launch_bounds__(256) k3da_combine_kernel(const __grid_constant__ Params p) {
-    __shared__ Plan pl;
-    build_plan(p, &pl, -1, 1, false);
-    __syncthreads();
+__global__ void __launch_bounds__(128) k3da_combine_kernel(const __grid_constant__ Params p) {
     const int per_unit = kRows / kCombineRows;
     const int u = blockIdx.x / per_unit;
-    const int row = (blockIdx.x - u * per_unit) * kCombineRows + (threadIdx.x >> 7);
-    const int dc = (threadIdx.x >> 4) & 7, sg = threadIdx.x & (kCombineLanes - 1);
+    const int row = (blockIdx.x - u * per_unit) * kCombineRows + (threadIdx.x >> 6);
+    const int dc = (threadIdx.x >> 3) & 7, sg = threadIdx.x & (kCombineLanes - 1);
     const int rows = kG * p.B;
-    const int nch = pl.nch[u];
-    const long long slot0 = pl.cstart[u];
+    if ((blockIdx.x - u * per_unit) * kCombineRows >= rows) return;  // whole CTA
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    const long long slot0 = p.ws_units[u];
+    const int nch = p.ws_units[kMaxUnits + u];
     float m = -INFINITY, l = 0.f;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (row < rows) {
@@ -1650,8 +1659,10 @@ size_t workspace_slots(int R, int Hkv, int page_stride) {
     return static_cast<size_t>(R) * Hkv * static_cast<size_t>(per_unit);
 }
 
+constexpr size_t kWsHeaderBytes = 512;  // unit table, then the partials (16-byte aligned)
+
 size_t workspace_for(int R, int Hkv, int page_stride) {
-    return workspace_slots(R, Hkv, page_stride) * (kPartialFloats * sizeof(float) + kRows * sizeof(float2));
+    return kWsHeaderBytes + workspace_slots(R, Hkv, page_stride) * (kPartialFloats * sizeof(float) + kRows * sizeof(float2));
 }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -1734,8 +1745,9 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
     prm.q_w = static_cast<const __nv_bfloat16 *>(q_norm_w);
     prm.k_w = static_cast<const __nv_bfloat16 *>(k_norm_w);
     const size_t slots = workspace_slots(R, Hkv, page_stride);
-    prm.ws_o = static_cast<float *>(workspace);
-    prm.ws_ml = reinterpret_cast<float2 *>(static_cast<float *>(workspace) + slots * kPartialFloats);
+    prm.ws_units = static_cast<int *>(workspace);
+    prm.ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + kWsHeaderBytes);
+    prm.ws_ml = reinterpret_cast<float2 *>(prm.ws_o + slots * kPartialFloats);
     prm.status = status;
     prm.num_pages = num_pages;
     prm.page_stride = page_stride;
@@ -1763,7 +1775,7 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
     cudaLaunchConfig_t lc;
     memset(&lc, 0, sizeof lc);
     lc.gridDim = dim3(static_cast<unsigned>(R * Hkv * (kRows / kCombineRows)));
-    lc.blockDim = dim3(256);
+    lc.blockDim = dim3(128);
     lc.dynamicSmemBytes = 0;
     lc.stream = st;
     cudaLaunchAttribute attr[1];

@@ -108,8 +108,11 @@ def test_workspace_query_refuses_bad_sizes(lib):
 
 def test_workspace_size_depends_on_shapes_only(lib):
     small = lib.k3da_workspace_bytes(1, 8, 6, 1, 32)
-    assert small > 0
-    assert lib.k3da_workspace_bytes(8, 8, 24, 4, 32) == 32 * small
+    two = lib.k3da_workspace_bytes(2, 8, 6, 1, 32)
+    assert small > 0 and two > small
+    per_unit = two - small  # a fixed header plus the same bytes per (request, kv head)
+    assert lib.k3da_workspace_bytes(8, 8, 24, 4, 32) == small + 31 * per_unit
+    assert lib.k3da_workspace_bytes(8, 8, 6, 1, 32) == lib.k3da_workspace_bytes(8, 1, 6, 1, 32)
     assert lib.k3da_workspace_bytes(8, 8, 24, 4, 2048) > lib.k3da_workspace_bytes(8, 8, 24, 4, 32)
 
 

@@ -75,7 +75,7 @@ constexpr int kChunkSplits = 16;   // a unit is cut into at most this many chunk
 #ifndef K3DA_CHUNK_MAX
 #define K3DA_CHUNK_MAX 32
 #endif
-constexpr int kChunkMax = K3DA_CHUNK_MAX;  // ... of at most this many items, beyond which it gets more chunks
+constexpr int kChunkMax = K3DA_CHUNK_MAX;  // ... of at most this many pages, beyond which it gets more chunks
 constexpr int kPartialFloats = kRows * kD;    // O of one (CTA, unit) range
 constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
@@ -260,8 +260,12 @@ __device__ __forceinline__ long long ceil_div_ll(long long a, long long b) { ret
 
 // Warp 0 reads and checks ctx_lens and builds the plan, one lane per unit
 // with shuffle scans; cta < 0 builds only the unit tables (for the
-// combine).  The caller syncs.
+// combine).  The caller syncs.  An item is the block (item 0) or a group of
+// G consecutive pages of the unit (the last group may be shorter); a chunk
+// holds at most kChunkMax / G items.
+template <int G>
 __device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool report) {
+    constexpr int kChunkItems = kChunkMax / G > 0 ? kChunkMax / G : 1;
     if (threadIdx.x >= 32) return;
     const int lane = threadIdx.x;
     int L = 0;
@@ -277,11 +281,12 @@ __device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool repor
     const int U = p.R * p.Hkv;
     const int u = lane;
     const int Lu = __shfl_sync(kFull, L, (u < U ? u / p.Hkv : 0));
-    int items = 0, ch = 1, nch = 0;
+    int items = 0, ch = 1, nch = 0, npages = 0;
     if (u < U) {
-        items = 1 + (Lu + kP - 1) / kP;
+        npages = (Lu + kP - 1) / kP;
+        items = 1 + (npages + G - 1) / G;
         ch = (items + kChunkSplits - 1) / kChunkSplits;
-        ch = ch < 1 ? 1 : (ch > kChunkMax ? kChunkMax : ch);
+        ch = ch < 1 ? 1 : (ch > kChunkItems ? kChunkItems : ch);
         nch = (items + ch - 1) / ch;
     }
     long long si = items;  // inclusive scans over units
@@ -323,8 +328,9 @@ __device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool repor
             j1 = static_cast<int>(b);
             const int i0 = j0 * ch;
             const int i1 = j1 * ch < items ? j1 * ch : items;
-            p0 = i0 == 0 ? 0 : i0 - 1;
-            npg = (i1 - 1) - p0;
+            p0 = i0 == 0 ? 0 : (i0 - 1) * G;
+            const int pe = (i1 - 1) * G < npages ? (i1 - 1) * G : npages;
+            npg = pe - p0;
         }
     }
     const unsigned mask = __ballot_sync(kFull, has);
@@ -521,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t bar_empty = bar_full + kStages * 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    build_plan(p, pl, blockIdx.x, p.grid, blockIdx.x == 0);
+    build_plan<1>(p, pl, blockIdx.x, p.grid, blockIdx.x == 0);
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         for (int s = 0; s < kStages; ++s) {
@@ -809,63 +815,88 @@ __global__ void __launch_bounds__(kThreads, 2)
 // ---------------------------------------------------- tcgen05 split pass --
 //
 // The same work plan, with the two contractions on the 5th-generation tensor
-// cores.  Warps 0..3 own the four 32-lane quarters of tensor memory (TMEM):
-// query row rho = 12*q + l (q = rho / 12 < 4, l < 12) is copied into Q-tile
-// rows (and TMEM lanes) 32*q + l and 32*q + 16 + l; the thread of the first
-// lane handles keys 0..31 of each page and the thread of the second keys
-// 32..63, so a row's softmax costs two threads half a page each and one
-// shuffle to share the row maximum.  Warp 4 streams K/V pages with TMA as
-// before; lane 0 of warp 5 issues the MMAs:
-//   S[b] (128 x 64 fp32, TMEM cols 64b..)  = Q (128 x 64, smem) . K_page^T
-//   O    (128 x 64 fp32, TMEM cols 128..) += P[b] (bf16, TMEM cols 192+32b..) . V_page
-// with two S buffers so the next page's QK^T overlaps this page's softmax.
+// cores.  An item is the block or a group of kGroup pages (1 by default; 2
+// gives one N = 128 QK^T per two pages but only one CTA per SM).  Row warps
+// w own TMEM lane quarter q = w % 4 (and page w / 4 of a group): query row
+// rho = 12*q + l (l < 12) is copied into Q-tile rows (and TMEM lanes)
+// 32*q + l and 32*q + 16 + l; the thread of the first lane handles keys
+// 0..31 of its page and the thread of the second keys 32..63, so a row's
+// softmax costs two threads half a page each and one shuffle to share the
+// row maximum.  The producer warp streams K/V pages with TMA; one warp issues
+// the QK^T products and another the P.V products (a thread issues one MMA
+// at a time, ~156 cycles each at these shapes whatever N, so two issuers
+// double the tensor throughput of a CTA):
+//   S[b] (128 x 64g fp32, TMEM)  = Q (128 x 64, smem) . K_group^T
+//   O    (128 x 64 fp32, TMEM)  += P[b] (bf16, TMEM) . V_page   (per page)
+// with two S buffers so the next item's QK^T overlaps this item's softmax.
 // The softmax keeps a per-row exponent base m; P = 2^(s*scale*log2e - m) is
-// written as bf16 to TMEM buffer P[b] (cols 192 + 32b; each lane's other
-// half of the keys as zeros; kept apart from S[b] so that the next QK^T into
-// S[b] never overwrites a P the previous PV may still be reading) and
-// becomes the A operand of the PV MMA, so each of a row's two lanes
-// accumulates its half of P.V; the halves are added when the chunk's
-// partial is written.  O is only rescaled when a row's maximum passes m by
-// more than 8 (log2 units; P <= 256 is exact enough in bf16 and fp32), so
-// the common path never touches O.
+// written as bf16 to TMEM buffer P[b] (each lane's other half of the keys as
+// zeros; kept apart from S[b] so that the next QK^T into S[b] never
+// overwrites a P the previous PV may still be reading) and becomes the A
+// operand of the PV MMA, so each of a row's two lanes accumulates its half
+// of P.V; the halves are added when the chunk's partial is written.  O is
+// only rescaled when a row's maximum passes m by more than 8 (log2 units;
+// P <= 256 is exact enough in bf16 and fp32), so the common path never
+// touches O.
 namespace tc {
+#ifndef K3DA_TC_GROUP
+#define K3DA_TC_GROUP 1
+#endif
+constexpr int kGroup = K3DA_TC_GROUP;  // pages per item
 #ifndef K3DA_TC_STAGES
-#define K3DA_TC_STAGES 4
+#define K3DA_TC_STAGES (K3DA_TC_GROUP == 1 ? 4 : 5)
 #endif
 constexpr int kStages = K3DA_TC_STAGES;
-constexpr int kRowWarps = 4;
+constexpr int kSets = kGroup;         // row-warp sets: set s takes page s of each group
+constexpr int kRowWarps = 4 * kSets;  // one warp per TMEM lane quarter and set
 constexpr int kRowThreads = 32 * kRowWarps;
 constexpr int kRowsPerQuarter = 12;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 32 * 6;
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColO = 128;
-constexpr uint32_t kColP = 192;  // P[b] at kColP + 32*b (bf16 pairs), apart from S[b]
+constexpr int kProducerWarp = kRowWarps;
+constexpr int kQkWarp = kRowWarps + 1;  // issues the QK^T products (and owns the TMEM allocation)
+constexpr int kPvWarp = kRowWarps + 2;  // issues the P.V products
+constexpr int kThreads = 32 * (kRowWarps + 3);
+constexpr int kDimsPerSet = kD / kSets;  // O columns each set rescales and writes
+constexpr int kGroupBytes = kGroup * kStageBytes;  // K tiles of the group's pages, then their V tiles
+// Tensor memory: S[b] (64 columns per page of the group) at kSCols*b, O,
+// then P[b] (32 columns of bf16 pairs per page) at kColP + kPCols*b.
+constexpr uint32_t kSCols = 64u * kGroup;
+constexpr uint32_t kColO = 2u * kSCols;
+constexpr uint32_t kColP = kColO + 64u;
+constexpr uint32_t kPCols = 32u * kGroup;
+constexpr uint32_t kTmemUsed = kColP + 2u * kPCols;
+constexpr uint32_t kTmemCols = kTmemUsed <= 256u ? 256u : 512u;
+static_assert(kTmemUsed <= 512u, "tensor memory holds 512 columns");
+constexpr int kCtasPerSm = kTmemCols == 256u ? 2 : 1;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // Shared memory (offsets from a 1024-byte aligned base).
-constexpr int kOffStages = 0;                        // kStages x (K 8 KB + V 8 KB)
-constexpr int kOffQ = kStages * kStageBytes;         // 128 rows x 128 B, 128B swizzle
+constexpr int kOffStages = 0;                        // kStages x kGroupBytes
+constexpr int kOffQ = kStages * kGroupBytes;         // 128 rows x 128 B, 128B swizzle
 constexpr int kOffBlkK = kOffQ + 128 * 128;          // 64 rows x 128 B
 constexpr int kOffBlkV = kOffBlkK + 64 * 128;        // 64 rows x 128 B
 constexpr int kOffRaw = kOffBlkV + 64 * 128;         // raw q [8][6][64], k [8][64], v [8][64]
 constexpr int kOffTrig = kOffRaw + kMaxB * (kG + 2) * kD * 2;  // [8][32] float2
 constexpr int kOffNormW = kOffTrig + kMaxB * 32 * 8;  // q and k norm weights, [2][64] float
-constexpr int kOffPlan = kOffNormW + 2 * kD * 4;
+constexpr int kOffXch = kOffNormW + 2 * kD * 4;      // row max [2][kSets][128], row sum [kSets][128]
+constexpr int kOffPlan = kOffXch + 3 * kSets * 128 * 4;
 constexpr int kNumBars = 2 * kStages + 7;  // full, empty, s_full[2], p_full[2], o_done, q_ready, done
 constexpr int kOffBar = kOffPlan + 1536;
 constexpr int kOffTaddr = kOffBar + kNumBars * 8;
 constexpr int kOffFlag = kOffTaddr + 8;
 constexpr int kSmemUsed = kOffFlag + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 static_assert(kOffQ % 1024 == 0 && kOffBlkK % 1024 == 0 && kOffBlkV % 1024 == 0, "SW128 tiles need 1 KB alignment");
 static_assert(kOffBar % 8 == 0 && kOffPlan % 8 == 0, "mbarrier / int64 alignment");
 
 // Instruction descriptor of kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9 = 1, 10-12 = 1), K-major A and B unless bit 16 makes B
 // MN-major, N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
-constexpr uint32_t kIdescPV = kIdescQK | (1u << 16);
+constexpr uint32_t idesc_f16(uint32_t m, uint32_t n, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? 1u << 16 : 0u) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+constexpr uint32_t kIdescQK = idesc_f16(128, 64 * kGroup, false);  // a page group's keys
+constexpr uint32_t kIdescQKBlock = idesc_f16(128, 64, false);       // the block tile
+constexpr uint32_t kIdescPV = idesc_f16(128, 64, true);
 
 // Shared-memory matrix descriptor of a tile stored in 128-byte rows with the
 // 128-byte swizzle (8-row, 1 KB atoms): start address >> 4 (bits 0-13),
@@ -919,17 +950,31 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 32 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 }  // namespace tc
 
 template <bool QKNORM>
-__global__ void __launch_bounds__(tc::kThreads, 2)
+__global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     k3da_tc_kernel(const __grid_constant__ CUtensorMap pool_map, const __grid_constant__ Params p) {
     constexpr auto kStages = tc::kStages;
+    constexpr auto kGroup = tc::kGroup;
+    constexpr auto kGroupBytes = tc::kGroupBytes;
+    constexpr auto kSCols = tc::kSCols;
+    constexpr auto kPCols = tc::kPCols;
+    constexpr auto kIdescQKBlock = tc::kIdescQKBlock;
     constexpr auto kRowWarps = tc::kRowWarps;
     constexpr auto kRowThreads = tc::kRowThreads;
     constexpr auto kRowsPerQuarter = tc::kRowsPerQuarter;
     constexpr auto kProducerWarp = tc::kProducerWarp;
-    constexpr auto kMmaWarp = tc::kMmaWarp;
+    constexpr auto kQkWarp = tc::kQkWarp;
+    constexpr auto kPvWarp = tc::kPvWarp;
     constexpr auto kThreads = tc::kThreads;
     constexpr auto kTmemCols = tc::kTmemCols;
     constexpr auto kColO = tc::kColO;
@@ -942,6 +987,9 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
     constexpr auto kOffRaw = tc::kOffRaw;
     constexpr auto kOffTrig = tc::kOffTrig;
     constexpr auto kOffNormW = tc::kOffNormW;
+    constexpr auto kOffXch = tc::kOffXch;
+    constexpr auto kSets = tc::kSets;
+    constexpr auto kDimsPerSet = tc::kDimsPerSet;
     constexpr auto kOffPlan = tc::kOffPlan;
     constexpr auto kNumBars = tc::kNumBars;
     constexpr auto kOffBar = tc::kOffBar;
@@ -956,6 +1004,7 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
     using tc::fence_before;
     using tc::fence_after;
     using tc::tmem_ld64;
+    using tc::tmem_ld32;
     using tc::tmem_st32;
     using tc::tmem_wait_st;
     extern __shared__ uint8_t smem_raw[];
@@ -970,7 +1019,7 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
     const uint32_t bar_odone = bar_pfull + 16, bar_qready = bar_odone + 8, bar_done = bar_qready + 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    build_plan(p, pl, blockIdx.x, p.grid, blockIdx.x == 0);
+    build_plan<tc::kGroup>(p, pl, blockIdx.x, p.grid, blockIdx.x == 0);
     {
         // Q and block tiles start as zeros: rows without a query row or a
         // block token stay zero for the whole kernel.
@@ -990,10 +1039,10 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
         mbar_init(bar_pfull + 8, kRowWarps);
         mbar_init(bar_odone, 1);
         mbar_init(bar_qready, kRowWarps);
-        mbar_init(bar_done, 1);
+        mbar_init(bar_done, 2);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == kMmaWarp) {
+    if (warp == kQkWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(taddr_slot)),
                      "r"(kTmemCols)
                      : "memory");
@@ -1013,6 +1062,10 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
 
     if (warp == kProducerWarp && nrun > 0) {
         // ------------------------------------------------ producer warp --
+        // The CTA's pages, run after run, form one sequence; lane l resolves
+        // entry base + l of each 32-entry batch (page id -> TMA row of its K
+        // tile, -1 if out of range), one batch ahead of the loads it feeds.
+        // Each stage takes one item: up to kGroup pages of one run.
         uint64_t policy;
         asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
         const int total = pl->run_pq[nrun];
@@ -1027,38 +1080,72 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
             if (page < 0 || page >= p.num_pages) return -1;  // served as zeros, flagged
             return ((page * 2 + 0) * p.Hkv + h) * kP;
         };
-        int next = resolve(lane);
-        for (int base = 0; base < total; base += 32) {
-            const int rows_k = next;
-            next = resolve(base + 32 + lane);
-            const int cnt = total - base < 32 ? total - base : 32;
-            for (int j = 0; j < cnt; ++j) {
-                const long long k = base + j;
-                const int krow = __shfl_sync(kFull, rows_k, j);
+        int base = 0, cur = resolve(lane), nxt = resolve(32 + lane);
+        int q = 0;
+        long long k = 0;  // items loaded
+        for (int rn = 0; rn < nrun; ++rn) {
+            const int npg = pl->run_pq[rn + 1] - pl->run_pq[rn];
+            for (int g0 = 0; g0 < npg; g0 += kGroup, ++k) {
+                const int cnt = npg - g0 < kGroup ? npg - g0 : kGroup;
+                int krow[kGroup];
+#pragma unroll
+                for (int j = 0; j < kGroup; ++j) {
+                    krow[j] = -2;  // no page
+                    if (j < cnt) {
+                        if (q >= base + 32) {
+                            base += 32;
+                            cur = nxt;
+                            nxt = resolve(base + 32 + lane);
+                        }
+                        krow[j] = __shfl_sync(kFull, cur, q - base);
+                        ++q;
+                    }
+                }
                 const int s = static_cast<int>(k % kStages);
                 const uint32_t par = static_cast<uint32_t>((k / kStages) & 1);
                 mbar_wait(bar_empty + 8 * s, par ^ 1u, abort_flag, p.status);
-                uint8_t *stage = smem + kOffStages + s * kStageBytes;
-                if (krow >= 0) {
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
-                        tma_load_tile(smem_u32(stage), &pool_map, krow, bar_full + 8 * s, policy);
-                        tma_load_tile(smem_u32(stage + kTileBytes), &pool_map, krow + p.Hkv * kP, bar_full + 8 * s,
-                                      policy);
+                uint8_t *stage = smem + kOffStages + s * kGroupBytes;
+                int bytes = 0;
+#pragma unroll
+                for (int j = 0; j < kGroup; ++j) {
+                    if (krow[j] >= 0) {
+                        bytes += kStageBytes;
+                    } else if (krow[j] == -1) {
+                        // Out-of-range page id: flag it and serve zeros.
+                        if (lane == 0 && p.status) atomicOr(p.status, K3DA_STATUS_BAD_PAGE);
+                        uint4 *dk = reinterpret_cast<uint4 *>(stage + j * kTileBytes);
+                        uint4 *dv = reinterpret_cast<uint4 *>(stage + (kGroup + j) * kTileBytes);
+                        for (int e = lane; e < kTileBytes / 16; e += 32) {
+                            dk[e] = make_uint4(0, 0, 0, 0);
+                            dv[e] = make_uint4(0, 0, 0, 0);
+                        }
                     }
-                } else {
-                    if (lane == 0 && p.status) atomicOr(p.status, K3DA_STATUS_BAD_PAGE);
-                    uint4 *dst = reinterpret_cast<uint4 *>(stage);
-                    for (int q = lane; q < kStageBytes / 16; q += 32) dst[q] = make_uint4(0, 0, 0, 0);
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_full + 8 * s);
+                }
+                if (bytes < cnt * kStageBytes) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    if (bytes > 0) {
+                        mbar_arrive_expect_tx(bar_full + 8 * s, bytes);
+#pragma unroll
+                        for (int j = 0; j < kGroup; ++j) {
+                            if (krow[j] >= 0) {
+                                tma_load_tile(smem_u32(stage + j * kTileBytes), &pool_map, krow[j], bar_full + 8 * s,
+                                              policy);
+                                tma_load_tile(smem_u32(stage + (kGroup + j) * kTileBytes), &pool_map,
+                                              krow[j] + p.Hkv * kP, bar_full + 8 * s, policy);
+                            }
+                        }
+                    } else {
+                        mbar_arrive(bar_full + 8 * s);
+                    }
                 }
                 __syncwarp();
             }
         }
+        // Drain: every issued load must land before the CTA exits (matters
+        // only when a wait gave up and the consumers stopped early).
         if (*abort_flag) {
-            for (long long j = (total > kStages ? total - kStages : 0); j < total; ++j) {
+            for (long long j = (k > kStages ? k - kStages : 0); j < k; ++j) {
                 const int s = static_cast<int>(j % kStages);
                 const uint32_t par = static_cast<uint32_t>((j / kStages) & 1);
                 const unsigned long long t0 = global_ns();
@@ -1066,73 +1153,93 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
                 }
             }
         }
-    } else if (warp == kMmaWarp && nrun > 0) {
-        // ---------------------------------------------------- MMA warp --
-        // Items run in order; the QK^T of item i+1 is issued before the PV
-        // of item i (within a run), so it overlaps item i's softmax.
+    } else if ((warp == kQkWarp || warp == kPvWarp) && nrun > 0) {
+        // ------------------------------------------------- MMA warps --
+        // A thread issues one tcgen05.mma at a time (about 156 cycles each at
+        // these shapes, whatever N), so the two products have an issuing
+        // warp each.  The QK^T warp fills S[b] for item i once the row warps
+        // have released it (item i-2 done); a page group's K tiles sit back
+        // to back, so its QK^T is one N = 64*kGroup product.  The P.V warp
+        // accumulates O once item i's P is in TMEM, one product per page
+        // present, then releases the stage (QK^T of the item completed
+        // before its softmax began).
+        const bool is_qk = warp == kQkWarp;
         const uint64_t q_desc = desc_sw128(smem_u32(smem + kOffQ));
         const uint64_t bk_desc = desc_sw128(smem_u32(smem + kOffBlkK));
         const uint64_t bv_desc = desc_sw128(smem_u32(smem + kOffBlkV));
         long long it = 0, kr = 0;
-        bool pend = false;
-        int pend_b = 0, pend_s = 0;
-        bool pend_page = false, pend_first = false;
-        long long pend_it = 0;
-        auto issue_pv = [&]() {
-            mbar_wait(bar_pfull + 8 * pend_b, static_cast<uint32_t>((pend_it >> 1) & 1), abort_flag, p.status);
-            fence_after();
-            if (lane == 0) {
-                const uint64_t v_desc =
-                    pend_page ? desc_sw128(smem_u32(smem + kOffStages + pend_s * kStageBytes + kTileBytes)) : bv_desc;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ts(tmem + kColO, tmem + kColP + 32u * pend_b + 8u * kk, v_desc + ((kk * 2048) >> 4), kIdescPV,
-                           (kk > 0 || !pend_first) ? 1u : 0u);
-                mma_commit(bar_odone);
-                if (pend_page) mma_commit(bar_empty + 8 * pend_s);
-            }
-            __syncwarp();
-        };
         for (int rn = 0; rn < nrun; ++rn) {
             const int u = pl->run_u[rn];
+            const int r = u / p.Hkv;
+            const int npages = (pl->lens[r] + kP - 1) / kP;
             const int ch = pl->ch[u];
             const int items = static_cast<int>(pl->ustart[u + 1] - pl->ustart[u]);
-            mbar_wait(bar_qready, static_cast<uint32_t>(rn & 1), abort_flag, p.status);
-            fence_after();
+            if (is_qk) {
+                mbar_wait(bar_qready, static_cast<uint32_t>(rn & 1), abort_flag, p.status);
+                fence_after();
+            }
             for (int jc = pl->run_j0[rn]; jc < pl->run_j1[rn]; ++jc) {
                 const int i0 = jc * ch;
                 const int i1 = i0 + ch < items ? i0 + ch : items;
-                for (int item = i0; item < i1; ++item) {
+                for (int item = i0; item < i1; ++item, ++it) {
                     const int b = static_cast<int>(it & 1);
                     const bool is_page = item > 0;
-                    const int s = static_cast<int>(kr % kStages);
+                    int cnt = 0;
                     if (is_page) {
-                        mbar_wait(bar_full + 8 * s, static_cast<uint32_t>((kr / kStages) & 1), abort_flag, p.status);
-                        fence_after();
+                        const int left = npages - (item - 1) * kGroup;
+                        cnt = left < kGroup ? left : kGroup;
                     }
-                    if (lane == 0) {
-                        const uint64_t k_desc = is_page ? desc_sw128(smem_u32(smem + kOffStages + s * kStageBytes))
-                                                        : bk_desc;
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tmem + 64u * b, q_desc + ((kk * 32) >> 4), k_desc + ((kk * 32) >> 4), kIdescQK,
-                                   kk > 0 ? 1u : 0u);
-                        mma_commit(bar_sfull + 8 * b);
-                    }
-                    __syncwarp();
-                    if (pend) issue_pv();
-                    pend = true;
-                    pend_b = b;
-                    pend_s = s;
-                    pend_page = is_page;
-                    pend_first = item == i0;
-                    pend_it = it;
-                    ++it;
+                    const int s = static_cast<int>(kr % kStages);
                     if (is_page) ++kr;
+                    if (is_qk) {
+                        if (it >= 2) {  // S[b] is free once item it-2's P is out
+                            mbar_wait(bar_pfull + 8 * b, static_cast<uint32_t>(((it - 2) >> 1) & 1), abort_flag,
+                                      p.status);
+                            fence_after();
+                        }
+                        if (is_page) {
+                            mbar_wait(bar_full + 8 * s, static_cast<uint32_t>(((kr - 1) / kStages) & 1), abort_flag,
+                                      p.status);
+                            fence_after();
+                        }
+                        if (lane == 0) {
+                            const uint64_t k_desc =
+                                is_page ? desc_sw128(smem_u32(smem + kOffStages + s * kGroupBytes)) : bk_desc;
+                            const uint32_t idesc = is_page ? kIdescQK : kIdescQKBlock;
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_ss(tmem + kSCols * b, q_desc + ((kk * 32) >> 4), k_desc + ((kk * 32) >> 4), idesc,
+                                       kk > 0 ? 1u : 0u);
+                            mma_commit(bar_sfull + 8 * b);
+                        }
+                        __syncwarp();
+                    } else {
+                        const bool first = item == i0;
+                        mbar_wait(bar_pfull + 8 * b, static_cast<uint32_t>((it >> 1) & 1), abort_flag, p.status);
+                        fence_after();
+                        if (lane == 0) {
+                            const uint32_t pcol = tmem + kColP + kPCols * b;
+                            if (cnt == 0) {
+                                // The block: at most 8 keys, all in the first 16-key step.
+                                mma_ts(tmem + kColO, pcol, bv_desc, kIdescPV, first ? 0u : 1u);
+                            } else {
+                                const uint32_t vbase =
+                                    smem_u32(smem + kOffStages + s * kGroupBytes + kGroup * kTileBytes);
+                                for (int pg = 0; pg < cnt; ++pg) {
+                                    const uint64_t v_desc = desc_sw128(vbase + pg * kTileBytes);
+#pragma unroll
+                                    for (int kk = 0; kk < 4; ++kk)
+                                        mma_ts(tmem + kColO, pcol + 32u * pg + 8u * kk, v_desc + ((kk * 2048) >> 4),
+                                               kIdescPV, (pg > 0 || kk > 0 || !first) ? 1u : 0u);
+                                }
+                            }
+                            mma_commit(bar_odone);
+                            if (cnt > 0) mma_commit(bar_empty + 8 * s);
+                        }
+                        __syncwarp();
+                    }
                 }
             }
-            if (pend) issue_pv();
-            pend = false;
         }
         if (lane == 0) mma_commit(bar_done);
         __syncwarp();
@@ -1141,14 +1248,20 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
         }
     } else if (warp < kRowWarps && nrun > 0) {
         // ------------------------------------------- softmax / row warps --
+        // Warp w serves TMEM lane quarter w % 4 and, within each page
+        // group, page w / 4 (its set).  The sets of a row share one
+        // exponent base: they swap their row maxima through shared memory
+        // at every item, and add their row sums at a chunk's end.
         const int t = threadIdx.x;
-        const int q = warp;
+        const int q = warp & 3;
+        const int set = warp >> 2;
         const int half = lane >> 4;               // key half of this lane
         const int l16 = lane & 15;
         const int rho = l16 < kRowsPerQuarter ? q * kRowsPerQuarter + l16 : 1 << 20;
         const int rows = kG * p.B;
         const bool active = rho < rows;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+        const int tl = 32 * q + lane;             // TMEM lane of this thread
         uint8_t *qtile = smem + kOffQ;
         uint8_t *bk = smem + kOffBlkK;
         uint8_t *bv = smem + kOffBlkV;
@@ -1156,9 +1269,11 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
         uint8_t *raw_k = raw_q + kMaxB * kG * kD * 2;
         uint8_t *raw_v = raw_k + kMaxB * kD * 2;
         float2 *trig = reinterpret_cast<float2 *>(smem + kOffTrig);
+        float *xmax = reinterpret_cast<float *>(smem + kOffXch);  // [2][kSets][128]
+        float *xsum = xmax + 2 * kSets * 128;                      // [kSets][128]
         const long long row_w = static_cast<long long>(p.Hq + 2 * p.Hkv) * kD;
         float *normw = reinterpret_cast<float *>(smem + kOffNormW);  // [0..63] q, [64..127] k
-        if (QKNORM) normw[t] = __bfloat162float(t < kD ? p.q_w[t] : p.k_w[t - kD]);
+        if (QKNORM && t < 2 * kD) normw[t] = __bfloat162float(t < kD ? p.q_w[t] : p.k_w[t - kD]);
         // A chunk's partial is written while the next chunk's first item is in
         // flight (its P.V, the last O reader, was confirmed just before), so
         // the wait for the chunk's last P.V hides behind that item's softmax.
@@ -1166,23 +1281,37 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
         long long epi_slot = 0;
         float epi_m = 0.f, epi_l = 0.f;
         auto write_partial = [&]() {
-            uint32_t orr[64];
-            tmem_ld64(tmem + lane_off + kColO, orr);
-            const float ltot = epi_l + __shfl_xor_sync(kFull, epi_l, 16);
-            float outv[32];
+            // Set s writes O columns [kDimsPerSet*s, +kDimsPerSet): lane half
+            // 0 the first half of them, half 1 the second, each adding the
+            // partner lane's share (the other half of the keys).
+            float ltot = epi_l + __shfl_xor_sync(kFull, epi_l, 16);
+            if (kSets > 1) {
+                xsum[set * 128 + tl] = ltot;
+                named_bar_sync(2, kRowThreads);
+                ltot = 0.f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                // lane half 0 keeps dims 0..31, half 1 dims 32..63.
-                const float give = __uint_as_float(half ? orr[j] : orr[32 + j]);
-                const float keep = __uint_as_float(half ? orr[32 + j] : orr[j]);
+                for (int s2 = 0; s2 < kSets; ++s2) ltot += xsum[s2 * 128 + tl];
+            }
+            constexpr int kKeep = kDimsPerSet / 2;
+            uint32_t orr[kDimsPerSet];
+#pragma unroll
+            for (int c = 0; c < kDimsPerSet / 32; ++c)
+                tmem_ld32(tmem + lane_off + kColO + kDimsPerSet * set + 32u * c,
+                          *reinterpret_cast<uint32_t(*)[32]>(orr + 32 * c));
+            float outv[kKeep];
+#pragma unroll
+            for (int j = 0; j < kKeep; ++j) {
+                const float give = __uint_as_float(half ? orr[j] : orr[kKeep + j]);
+                const float keep = __uint_as_float(half ? orr[kKeep + j] : orr[j]);
                 outv[j] = keep + __shfl_xor_sync(kFull, give, 16);
             }
             if (active) {
-                float4 *dst = reinterpret_cast<float4 *>(p.ws_o + epi_slot * kPartialFloats + rho * kD + 32 * half);
+                float4 *dst = reinterpret_cast<float4 *>(p.ws_o + epi_slot * kPartialFloats + rho * kD +
+                                                         kDimsPerSet * set + kKeep * half);
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
+                for (int j = 0; j < kKeep / 4; ++j)
                     dst[j] = make_float4(outv[4 * j], outv[4 * j + 1], outv[4 * j + 2], outv[4 * j + 3]);
-                if (half == 0) p.ws_ml[epi_slot * kRows + rho] = make_float2(epi_m, ltot);
+                if (half == 0 && set == 0) p.ws_ml[epi_slot * kRows + rho] = make_float2(epi_m, ltot);
             }
             epi_pending = false;
         };
@@ -1238,6 +1367,12 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
                 }
             }
             cp_async_wait_all();
+            if (it > 0) {
+                // The block tiles are rewritten below: the last P.V (which
+                // may have read the previous block's V) must be complete.
+                mbar_wait(bar_odone, static_cast<uint32_t>((it - 1) & 1), abort_flag, p.status);
+                fence_after();
+            }
             named_bar_sync(1, kRowThreads);
             // Two threads per row: thread t takes row t/2 and the 16 RoPE
             // pairs (j, j+32) with j in [16*(t&1), 16*(t&1)+16).  Rows 0..47
@@ -1342,21 +1477,24 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
                     const int b = static_cast<int>(it & 1);
                     const bool is_page = item > 0;
                     const int s = static_cast<int>(kr % kStages);
+                    constexpr int kKeys = kP * kGroup;  // keys of a page group
                     int valid = p.B;
                     if (is_page) {
-                        const int left = L - (item - 1) * kP;
-                        valid = left < kP ? left : kP;
+                        const int left = L - (item - 1) * kKeys;
+                        valid = left < kKeys ? left : kKeys;
                     }
                     mbar_wait(bar_sfull + 8 * b, static_cast<uint32_t>((it >> 1) & 1), abort_flag, p.status);
                     fence_after();
-                    uint32_t sr[64];
-                    tmem_ld64(tmem + lane_off + 64u * b, sr);
-                    // This lane's half of the keys.
+                    // This lane's half of the keys of page `set` of the group.
                     float sv[32];
+                    {
+                        uint32_t sr[64];
+                        tmem_ld64(tmem + lane_off + kSCols * b + 64u * set, sr);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(half ? sr[32 + j] : sr[j]);
-                    if (valid < kP) {
-                        const int lim = valid - 32 * half;
+                        for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(half ? sr[32 + j] : sr[j]);
+                    }
+                    if (valid < kKeys) {
+                        const int lim = valid - 64 * set - 32 * half;
 #pragma unroll
                         for (int j = 0; j < 32; ++j) sv[j] = j < lim ? sv[j] : -INFINITY;
                     }
@@ -1367,31 +1505,43 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
                     for (int j = 4; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], sv[j]);
                     float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                     rmax = fmaxf(rmax, __shfl_xor_sync(kFull, rmax, 16)) * p.scale_log2;
+                    if (kSets > 1) {
+                        // Row max over the sets (key 0 of page 0 is always
+                        // valid, so the result is finite).
+                        float *xm = xmax + (it & 1) * kSets * 128;
+                        xm[set * 128 + tl] = rmax;
+                        named_bar_sync(2, kRowThreads);
+#pragma unroll
+                        for (int s2 = 0; s2 < kSets; ++s2) rmax = fmaxf(rmax, xm[s2 * 128 + tl]);
+                    }
                     // Exponent base: the row max on a chunk's first item; later,
                     // only when the max passes the base by more than 2^8.
                     const bool first = item == i0;
                     const bool need = !first && rmax > m_used + kRescaleThreshold;
                     const float m_new = (first || need) ? rmax : m_used;
                     const float f = need ? exp2_approx(m_used - m_new) : 1.f;
-                    uint32_t pk[16];
                     float rs[4] = {0.f, 0.f, 0.f, 0.f};
+                    {
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float p0 = exp2_approx(fmaf(sv[2 * j], p.scale_log2, -m_new));
-                        const float p1 = exp2_approx(fmaf(sv[2 * j + 1], p.scale_log2, -m_new));
-                        rs[j & 3] += p0 + p1;
-                        pk[j] = pack_bf16(p0, p1);
+                        for (int j = 0; j < 16; ++j) {
+                            const float p0 = exp2_approx(fmaf(sv[2 * j], p.scale_log2, -m_new));
+                            const float p1 = exp2_approx(fmaf(sv[2 * j + 1], p.scale_log2, -m_new));
+                            rs[j & 3] += p0 + p1;
+                            pk[j] = pack_bf16(p0, p1);
+                        }
+                        // P row of this lane for page `set`: its half of the
+                        // keys, zeros in the other half.
+                        uint32_t prow[32];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            prow[j] = half ? 0u : pk[j];
+                            prow[16 + j] = half ? pk[j] : 0u;
+                        }
+                        tmem_st32(tmem + lane_off + kColP + kPCols * b + 32u * set, prow);
                     }
                     lsum = (first ? 0.f : lsum * f) + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
                     m_used = m_new;
-                    // P row of this lane: its half of the keys, zeros elsewhere.
-                    uint32_t prow[32];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        prow[j] = half ? 0u : pk[j];
-                        prow[16 + j] = half ? pk[j] : 0u;
-                    }
-                    tmem_st32(tmem + lane_off + kColP + 32u * b, prow);
                     tmem_wait_st();
                     // The previous item's PV must be complete before O may be
                     // touched; confirming it at every item also keeps this
@@ -1402,22 +1552,26 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
                     }
                     if (epi_pending) write_partial();  // before this item's P.V overwrites O
                     if (__any_sync(kFull, need)) {
-                        uint32_t orr[64];
-                        tmem_ld64(tmem + lane_off + kColO, orr);
-                        uint32_t part[32];
+                        // Each set rescales its own O columns.
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) part[j] = __float_as_uint(__uint_as_float(orr[j]) * f);
-                        tmem_st32(tmem + lane_off + kColO, part);
+                        for (int c = 0; c < kDimsPerSet / 32; ++c) {
+                            const uint32_t col = tmem + lane_off + kColO + kDimsPerSet * set + 32u * c;
+                            uint32_t part[32];
+                            tmem_ld32(col, part);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) part[j] = __float_as_uint(__uint_as_float(orr[32 + j]) * f);
-                        tmem_st32(tmem + lane_off + kColO + 32u, part);
+                            for (int j = 0; j < 32; ++j) part[j] = __float_as_uint(__uint_as_float(part[j]) * f);
+                            tmem_st32(col, part);
+                        }
                         tmem_wait_st();
                     }
-                    if (is_page && valid < kP) {
+                    if (is_page && (valid & (kP - 1)) != 0) {
                         // Stale pool slots past the context may hold
-                        // non-finite values: zero them before P.V reads them.
-                        uint4 *vt = reinterpret_cast<uint4 *>(smem + kOffStages + s * kStageBytes + kTileBytes);
-                        for (int e = t; e < (kP - valid) * 8; e += kRowThreads) vt[valid * 8 + e] = make_uint4(0, 0, 0, 0);
+                        // non-finite values: zero them in the group's last
+                        // page before P.V reads them.
+                        const int lp = valid / kP, lv = valid - lp * kP;
+                        uint4 *vt = reinterpret_cast<uint4 *>(smem + kOffStages + s * kGroupBytes +
+                                                              (kGroup + lp) * kTileBytes);
+                        for (int e = t; e < (kP - lv) * 8; e += kRowThreads) vt[lv * 8 + e] = make_uint4(0, 0, 0, 0);
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     }
                     fence_before();
@@ -1444,7 +1598,7 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
     fence_before();
     __syncthreads();
     fence_after();
-    if (warp == kMmaWarp)
+    if (warp == kQkWarp)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -1551,10 +1705,12 @@ __global__ void __launch_bounds__(128) k3da_combine_kernel(const __grid_constant
 #if K3DA_USE_TCGEN05
 constexpr int kSplitThreads = tc::kThreads;
 constexpr int kSplitSmem = tc::kSmemBytes;
+constexpr int kSplitGroup = tc::kGroup;
 #define kSplitLaunch k3da_tc_kernel
 #else
 constexpr int kSplitThreads = kThreads;
 constexpr int kSplitSmem = kSmemBytes;
+constexpr int kSplitGroup = 1;
 #define kSplitLaunch k3da_split_kernel
 #endif
 const void *const kSplitKernel[2] = {reinterpret_cast<const void *>(&kSplitLaunch<false>),
@@ -1651,10 +1807,12 @@ int configure_device(int dev, DeviceConfig *cfg) {
 
 bool supported_heads(int hq, int hkv) { return (hq == 6 && hkv == 1) || (hq == 24 && hkv == 4); }
 
-// Chunks a unit can have: at most kChunkSplits, or ceil(items/kChunkMax)
-// once chunks reach kChunkMax items; items <= page_stride + 1.
+// Chunks a unit can have: at most kChunkSplits, or ceil(items/ch_max) once
+// chunks reach ch_max = kChunkMax / G items; items <= 1 + ceil(page_stride / G).
 size_t workspace_slots(int R, int Hkv, int page_stride) {
-    const long long by_len = (static_cast<long long>(page_stride) + 1 + kChunkMax - 1) / kChunkMax;
+    constexpr long long ch_max = kChunkMax / kSplitGroup > 0 ? kChunkMax / kSplitGroup : 1;
+    const long long items = 1 + (static_cast<long long>(page_stride) + kSplitGroup - 1) / kSplitGroup;
+    const long long by_len = (items + ch_max - 1) / ch_max;
     const long long per_unit = by_len > kChunkSplits ? by_len : kChunkSplits;
     return static_cast<size_t>(R) * Hkv * static_cast<size_t>(per_unit);
 }

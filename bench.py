@@ -383,7 +383,7 @@ def run_ours(args, world, rank):
     achieved = split_bytes / (split_us * 1e-6) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
-                "kernel": "k3da_split_kernel (split pass; combine excluded)",
+                "kernel": "k3da_tc_kernel (split pass; combine excluded)",
                 "algorithmic_bytes_per_launch": split_bytes, "launch_us": split_us,
                 "peak_source": peak_src,
                 "combine_us_unoverlapped": statistics.mean(combine_ms) * 1e3,

@@ -878,7 +878,7 @@ constexpr int kOffTrig = kOffRaw + kMaxB * (kG + 2) * kD * 2;  // [8][32] float2
 constexpr int kOffNormW = kOffTrig + kMaxB * 32 * 8;  // q and k norm weights, [2][64] float
 constexpr int kOffXch = kOffNormW + 2 * kD * 4;      // row max [2][kSets][128], row sum [kSets][128]
 constexpr int kOffPlan = kOffXch + 3 * kSets * 128 * 4;
-constexpr int kNumBars = 2 * kStages + 7;  // full, empty, s_full[2], p_full[2], o_done, q_ready, done
+constexpr int kNumBars = 2 * kStages + 8;  // full, empty, s_full[2], p_full[2], o_done[2], q_ready, done
 constexpr int kOffBar = kOffPlan + 1536;
 constexpr int kOffTaddr = kOffBar + kNumBars * 8;
 constexpr int kOffFlag = kOffTaddr + 8;
@@ -1016,7 +1016,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     const uint32_t bars = smem_u32(smem + kOffBar);
     const uint32_t bar_full = bars, bar_empty = bars + 8 * kStages;
     const uint32_t bar_sfull = bars + 16 * kStages, bar_pfull = bar_sfull + 16;
-    const uint32_t bar_odone = bar_pfull + 16, bar_qready = bar_odone + 8, bar_done = bar_qready + 8;
+    const uint32_t bar_odone = bar_pfull + 16, bar_qready = bar_odone + 16, bar_done = bar_qready + 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     build_plan<tc::kGroup>(p, pl, blockIdx.x, p.grid, blockIdx.x == 0);
@@ -1038,6 +1038,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         mbar_init(bar_pfull, kRowWarps);
         mbar_init(bar_pfull + 8, kRowWarps);
         mbar_init(bar_odone, 1);
+        mbar_init(bar_odone + 8, 1);
         mbar_init(bar_qready, kRowWarps);
         mbar_init(bar_done, 2);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1233,7 +1234,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                                                kIdescPV, (pg > 0 || kk > 0 || !first) ? 1u : 0u);
                                 }
                             }
-                            mma_commit(bar_odone);
+                            mma_commit(bar_odone + 8 * b);  // o_done[it & 1]
                             if (cnt > 0) mma_commit(bar_empty + 8 * s);
                         }
                         __syncwarp();
@@ -1370,7 +1371,8 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
             if (it > 0) {
                 // The block tiles are rewritten below: the last P.V (which
                 // may have read the previous block's V) must be complete.
-                mbar_wait(bar_odone, static_cast<uint32_t>((it - 1) & 1), abort_flag, p.status);
+                mbar_wait(bar_odone + 8 * static_cast<uint32_t>((it - 1) & 1),
+                          static_cast<uint32_t>(((it - 1) >> 1) & 1), abort_flag, p.status);
                 fence_after();
             }
             named_bar_sync(1, kRowThreads);
@@ -1543,11 +1545,17 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                     lsum = (first ? 0.f : lsum * f) + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
                     m_used = m_new;
                     tmem_wait_st();
-                    // The previous item's PV must be complete before O may be
-                    // touched; confirming it at every item also keeps this
-                    // thread within one phase of o_done.
-                    if (it > 0) {
-                        mbar_wait(bar_odone, static_cast<uint32_t>((it - 1) & 1), abort_flag, p.status);
+                    // O is touched (a chunk's partial, a rescale) only once the
+                    // previous item's P.V is complete; otherwise P is handed
+                    // over at once and that P.V is confirmed after the
+                    // hand-over.  Item i's P.V completes phase i/2 of
+                    // o_done[i & 1], whose next phase needs item i+2's P, so
+                    // the confirmation cannot be overtaken.
+                    const bool touch_o = epi_pending || __any_sync(kFull, need);
+                    const uint32_t od_bar = bar_odone + 8 * static_cast<uint32_t>((it - 1) & 1);
+                    const uint32_t od_par = static_cast<uint32_t>(((it - 1) >> 1) & 1);
+                    if (touch_o && it > 0) {
+                        mbar_wait(od_bar, od_par, abort_flag, p.status);
                         fence_after();
                     }
                     if (epi_pending) write_partial();  // before this item's P.V overwrites O
@@ -1577,6 +1585,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                     fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_pfull + 8 * b);
+                    if (!touch_o && it > 0) mbar_wait(od_bar, od_par, abort_flag, p.status);
                     ++it;
                     if (is_page) ++kr;
                 }
@@ -1588,7 +1597,8 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
             }
         }
         if (epi_pending) {
-            mbar_wait(bar_odone, static_cast<uint32_t>((it - 1) & 1), abort_flag, p.status);
+            mbar_wait(bar_odone + 8 * static_cast<uint32_t>((it - 1) & 1), static_cast<uint32_t>(((it - 1) >> 1) & 1),
+                      abort_flag, p.status);
             fence_after();
             write_partial();
         }

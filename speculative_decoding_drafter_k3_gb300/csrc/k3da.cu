@@ -13,8 +13,9 @@
 // Design (one GPU, HBM-bound):
 //   * Work unit = (request r, kv head h).  Its items are the block (item 0,
 //     the B block keys) and its context pages (items 1..ceil(L/64)).  A unit
-//     is cut into chunks of ch(u) items, ch(u) = clamp(ceil(items/16), 1,
-//     kChunkMax), so chunk boundaries depend on that unit's length alone.
+//     is cut into chunks of ch(u) items, ch(u) = clamp(ceil(items/n), 1,
+//     kChunkMax) with n = max(16, ceil(304/units)), so chunk boundaries
+//     depend on that unit's length and the call's shape alone.
 //     All units' items are laid end to end; CTA c of the grid (sized to fill
 //     every SM) takes the chunks whose first item falls in the c-th equal
 //     slice of that line.  Long and short contexts thus spread over all SMs,
@@ -72,6 +73,7 @@ constexpr int kStageBytes = 2 * kTileBytes;   // K + V
 constexpr int kStages = K3DA_STAGES;
 constexpr int kMaxCtasPerSm = 2;
 constexpr int kChunkSplits = 16;   // a unit is cut into at most this many chunks ...
+constexpr int kChunkTarget = 304;  // ... or, with few units, about this many chunks in all
 #ifndef K3DA_CHUNK_MAX
 #define K3DA_CHUNK_MAX 32
 #endif
@@ -258,6 +260,14 @@ static_assert(sizeof(Plan) <= 1536, "plan fits its shared-memory slot");
 
 __device__ __forceinline__ long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
 
+// Chunks a unit is cut into (before the kChunkMax cap): 16, or more when
+// there are few units so that a single request still spreads over the GPU.
+// A function of the call's shape only, never of the lengths, so a chunk's
+// partial does not depend on other requests.
+__host__ __device__ constexpr int chunk_splits(int units) {
+    return (kChunkTarget + units - 1) / units > kChunkSplits ? (kChunkTarget + units - 1) / units : kChunkSplits;
+}
+
 // Warp 0 reads and checks ctx_lens and builds the plan, one lane per unit
 // with shuffle scans; cta < 0 builds only the unit tables (for the
 // combine).  The caller syncs.  An item is the block (item 0) or a group of
@@ -282,10 +292,17 @@ __device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool repor
     const int u = lane;
     const int Lu = __shfl_sync(kFull, L, (u < U ? u / p.Hkv : 0));
     int items = 0, ch = 1, nch = 0, npages = 0;
+    const int splits = chunk_splits(U);
     if (u < U) {
         npages = (Lu + kP - 1) / kP;
         items = 1 + (npages + G - 1) / G;
-        ch = (items + kChunkSplits - 1) / kChunkSplits;
+        // Finer chunks for few units, but never below the 16-way split's
+        // chunk or 4 items, whichever is smaller: short units keep the
+        // chunking of the 16-way split.
+        ch = (items + splits - 1) / splits;
+        const int ch16 = (items + kChunkSplits - 1) / kChunkSplits;
+        const int floor_ch = ch16 < 4 ? ch16 : 4;
+        ch = ch > floor_ch ? ch : floor_ch;
         ch = ch < 1 ? 1 : (ch > kChunkItems ? kChunkItems : ch);
         nch = (items + ch - 1) / ch;
     }
@@ -1817,13 +1834,14 @@ int configure_device(int dev, DeviceConfig *cfg) {
 
 bool supported_heads(int hq, int hkv) { return (hq == 6 && hkv == 1) || (hq == 24 && hkv == 4); }
 
-// Chunks a unit can have: at most kChunkSplits, or ceil(items/ch_max) once
-// chunks reach ch_max = kChunkMax / G items; items <= 1 + ceil(page_stride / G).
+// Chunks a unit can have: at most chunk_splits(R*Hkv), or ceil(items/ch_max)
+// once chunks reach ch_max = kChunkMax / G items; items <= 1 + ceil(page_stride / G).
 size_t workspace_slots(int R, int Hkv, int page_stride) {
     constexpr long long ch_max = kChunkMax / kSplitGroup > 0 ? kChunkMax / kSplitGroup : 1;
     const long long items = 1 + (static_cast<long long>(page_stride) + kSplitGroup - 1) / kSplitGroup;
     const long long by_len = (items + ch_max - 1) / ch_max;
-    const long long per_unit = by_len > kChunkSplits ? by_len : kChunkSplits;
+    const long long splits = chunk_splits(R * Hkv);
+    const long long per_unit = by_len > splits ? by_len : splits;
     return static_cast<size_t>(R) * Hkv * static_cast<size_t>(per_unit);
 }
 

@@ -143,7 +143,7 @@ def build_case(name: str, *, R: int, B: int, Hq: int, Hkv: int, lens: Sequence[i
     return case.to(device)
 
 
-# ---- the five workloads ---------------------------------------------------
+# ---- the workloads ---------------------------------------------------------
 
 SPLITS = [(1, 8), (2, 4), (4, 2), (8, 1), (3, 5), (5, 3), (8, 8), (6, 6)]
 SWEEP_LENGTHS = [0, 1, 63, 64, 65, 1000, 2041]
@@ -200,10 +200,38 @@ def long_context_small(device="cpu", seed: int = 4) -> Case:
     return long_context(device=device, seed=seed, num_pages=4096, lo=16384, hi=24576, page_stride=384)
 
 
+def w6_8x6(device="cpu", seed: int = 5) -> Case:
+    """The production draft block width W = 6: 8 requests x 6 tokens, 6/1
+    heads (36 query rows per kv head), fused, int32 positions, lengths
+    U{0..2041}, dense rows of a 4096-page pool."""
+    g = _gen(seed + 401, "cpu")
+    lens = torch.randint(0, 2042, (8,), generator=g).tolist()
+    return build_case("w6_8x6_6/1_L0-2041", R=8, B=6, Hq=6, Hkv=1, lens=lens, page_stride=32,
+                      num_pages=4096, qknorm=True, pos_dtype=torch.int32, seed=seed, device=device)
+
+
+def single_w6(device="cpu", seed: int = 6, L: int = 2041, Hq: int = 6, Hkv: int = 1,
+              page_stride: int = 32, num_pages: int = 4096) -> Case:
+    """One request with a W = 6 block (the single-request case), fused,
+    int64 positions; 6/1 heads and a 2041-token context by default."""
+    return build_case(f"single_1x6_{Hq}/{Hkv}_L{L}", R=1, B=6, Hq=Hq, Hkv=Hkv, lens=[L],
+                      page_stride=page_stride, num_pages=num_pages, qknorm=True,
+                      pos_dtype=torch.int64, seed=seed, device=device)
+
+
+def single_w6_long(device="cpu", seed: int = 7) -> Case:
+    """One request, W = 6 block, 24/4 heads, a 32768-token context (512
+    pages of a 4096-page pool)."""
+    return single_w6(device=device, seed=seed, L=32768, Hq=24, Hkv=4, page_stride=512, num_pages=4096)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "mixed_8x8": mixed_8x8,
     "heads_24_4": heads_24_4,
     "long_context": long_context,
     "long_context_small": long_context_small,
+    "w6_8x6": w6_8x6,
+    "single_w6": single_w6,
+    "single_w6_long": single_w6_long,
 }

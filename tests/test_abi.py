@@ -107,13 +107,19 @@ def test_workspace_query_refuses_bad_sizes(lib):
 
 
 def test_workspace_size_depends_on_shapes_only(lib):
-    small = lib.k3da_workspace_bytes(1, 8, 6, 1, 32)
-    two = lib.k3da_workspace_bytes(2, 8, 6, 1, 32)
-    assert small > 0 and two > small
-    per_unit = two - small  # a fixed header plus the same bytes per (request, kv head)
-    assert lib.k3da_workspace_bytes(8, 8, 24, 4, 32) == small + 31 * per_unit
-    assert lib.k3da_workspace_bytes(8, 8, 6, 1, 32) == lib.k3da_workspace_bytes(8, 1, 6, 1, 32)
-    assert lib.k3da_workspace_bytes(8, 8, 24, 4, 2048) > lib.k3da_workspace_bytes(8, 8, 24, 4, 32)
+    ws = lib.k3da_workspace_bytes
+    assert ws(1, 8, 6, 1, 32) > 0
+    # Block length never changes it; it grows with the page stride and the
+    # number of (request, kv head) units once chunks reach their maximum.
+    for R, Hq, Hkv in [(1, 6, 1), (8, 6, 1), (3, 24, 4), (8, 24, 4)]:
+        assert ws(R, 8, Hq, Hkv, 32) == ws(R, 1, Hq, Hkv, 32) == ws(R, 5, Hq, Hkv, 32)
+        assert ws(R, 8, Hq, Hkv, 2048) >= ws(R, 8, Hq, Hkv, 512) >= ws(R, 8, Hq, Hkv, 32)
+    assert ws(8, 8, 24, 4, 2048) > ws(8, 8, 24, 4, 512) > ws(8, 8, 24, 4, 32)
+    assert ws(8, 8, 24, 4, 2048) > ws(1, 8, 24, 4, 2048)
+    # With long rows every unit has ceil((stride+1)/32) slots of the same size.
+    slot = (ws(8, 8, 24, 4, 4096 - 1) - ws(8, 8, 24, 4, 2048 - 1)) // (32 * (128 - 64))
+    assert slot == 48 * 64 * 4 + 48 * 8
+    assert ws(8, 8, 24, 4, 2048 - 1) - ws(4, 8, 24, 4, 2048 - 1) == 16 * 64 * slot
 
 
 def test_product_path_does_not_touch_the_oracle():

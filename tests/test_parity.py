@@ -79,6 +79,15 @@ def test_large_positions_keep_rope_angles_exact():
     check(case)
 
 
+def test_production_block_width_w6_8x6():
+    check(workloads.w6_8x6(device="cuda"))
+
+
+@pytest.mark.parametrize("maker", [workloads.single_w6, workloads.single_w6_long])
+def test_single_request_w6(maker):
+    check(maker(device="cuda"))
+
+
 def test_long_context_sampled_requests():
     """The long-context workload at full size (20k-page pool, 16k..128k
     contexts, 24/4 heads), in the launch configuration the benchmark uses;

@@ -64,6 +64,11 @@ def _load():
                 ctypes.c_double, ctypes.c_double,
             ]
             lib.k3o_attn.restype = ctypes.c_int
+            lib.k3o_qk_norm_rope.argtypes = [
+                vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp,
+                ctypes.c_double, ctypes.c_double,
+            ]
+            lib.k3o_qk_norm_rope.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -155,6 +160,31 @@ def attn(qkv, pool, page_table, ctx_lens, *, num_requests: int, block_len: int,
             raise ValueError(f"oracle refused the inputs (status {st})")
         return out
     return out, st
+
+
+def qk_norm_rope(qkv, positions, q_norm_w, k_norm_w, *, num_q_heads: int, num_kv_heads: int,
+                 head_dim: int = 64, eps: float = 1e-5, rope_base: float = 10000.0) -> np.ndarray:
+    """The fused q/k norm + RoPE cell in fp64: ``[T, (Hq+2Hkv)*D]`` float64
+    with q and k heads normalised and rotated at their token's position and
+    v heads copied.  ``qkv``, ``q_norm_w``, ``k_norm_w`` are bf16; positions
+    of any integer type."""
+    lib = _load()
+    Hq, Hkv, D = num_q_heads, num_kv_heads, head_dim
+    qkv_b = bf16_bits(qkv).reshape(-1)
+    W = (Hq + 2 * Hkv) * D
+    assert qkv_b.shape[0] % W == 0
+    T = qkv_b.shape[0] // W
+    pos = np.ascontiguousarray(np.asarray(_np(positions)).astype(np.int64).reshape(-1))
+    assert pos.shape[0] == T
+    qw = bf16_bits(q_norm_w).reshape(-1)
+    kw = bf16_bits(k_norm_w).reshape(-1)
+    assert qw.shape[0] == D and kw.shape[0] == D
+    out = np.zeros((T, W), dtype=np.float64)
+    st = lib.k3o_qk_norm_rope(_ptr(out), _ptr(qkv_b), T, Hq, Hkv, D, _ptr(pos), _ptr(qw), _ptr(kw),
+                              float(eps), float(rope_base))
+    if st != OK:
+        raise ValueError(f"oracle refused the inputs (status {st})")
+    return out
 
 
 def _np(a):

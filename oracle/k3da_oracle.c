@@ -226,3 +226,53 @@ int k3o_attn(double *out, const uint16_t *qkv, const uint16_t *pool,
     free(wq); free(wk); free(raw); free(tmp); free(q);
     return status;
 }
+
+/*
+ * The drafter's fused q/k norm + RoPE cell on its own (the fused_qk_norm_rope
+ * cell of the commit adding the ops' contracts), for T tokens of qkv:
+ *
+ *   out        [T, (Hq + 2*Hkv)*D] fp64, written: query head rows become
+ *              rope(rmsnorm(q, q_w), pos_t), key head rows
+ *              rope(rmsnorm(k, k_w), pos_t), value head rows are copied
+ *   qkv        [T, (Hq + 2*Hkv)*D] bf16 bits (the layout of k3o_attn)
+ *   positions  [T] int64
+ *   q_w, k_w   [D] bf16 bits
+ *
+ * Returns K3O_OK, K3O_BAD_SHAPE or K3O_NO_MEMORY.
+ */
+int k3o_qk_norm_rope(double *out, const uint16_t *qkv, int T, int Hq, int Hkv, int D,
+                     const int64_t *positions, const uint16_t *q_w, const uint16_t *k_w,
+                     double eps, double base)
+{
+    if (T < 1 || Hq < 1 || Hkv < 1 || D < 2 || (D % 2) != 0)
+        return K3O_BAD_SHAPE;
+    const int heads = Hq + 2 * Hkv;
+    double *wq = (double *)malloc(sizeof(double) * (size_t)D);
+    double *wk = (double *)malloc(sizeof(double) * (size_t)D);
+    double *raw = (double *)malloc(sizeof(double) * (size_t)D);
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)D);
+    if (!wq || !wk || !raw || !tmp) {
+        free(wq); free(wk); free(raw); free(tmp);
+        return K3O_NO_MEMORY;
+    }
+    for (int j = 0; j < D; ++j) {
+        wq[j] = bf16_bits_to_f64(q_w[j]);
+        wk[j] = bf16_bits_to_f64(k_w[j]);
+    }
+    for (int t = 0; t < T; ++t) {
+        for (int h = 0; h < heads; ++h) {
+            const uint16_t *src = qkv + ((size_t)t * heads + h) * D;
+            double *dst = out + ((size_t)t * heads + h) * D;
+            for (int j = 0; j < D; ++j)
+                raw[j] = bf16_bits_to_f64(src[j]);
+            if (h < Hq + Hkv) {
+                k3o_rmsnorm(raw, h < Hq ? wq : wk, D, eps, tmp);
+                k3o_rope_neox(tmp, D, (double)positions[t], base, dst);
+            } else {
+                memcpy(dst, raw, sizeof(double) * (size_t)D);
+            }
+        }
+    }
+    free(wq); free(wk); free(raw); free(tmp);
+    return K3O_OK;
+}

@@ -27,6 +27,10 @@ MUTANTS = {
     "block_k_position_of_first_token": ("k3o_rope_neox(tmp, D, (double)positions[t], base, kdst);",
                                         "k3o_rope_neox(tmp, D, (double)positions[(int64_t)r * B], base, kdst);"),
     "k_normed_with_q_weight": ("k3o_rmsnorm(raw, wk, D, eps, tmp);", "k3o_rmsnorm(raw, wq, D, eps, tmp);"),
+    "cell_k_heads_with_q_weight": ("k3o_rmsnorm(raw, h < Hq ? wq : wk, D, eps, tmp);",
+                                   "k3o_rmsnorm(raw, wq, D, eps, tmp);"),
+    "cell_v_heads_normalised": ("if (h < Hq + Hkv) {", "if (h < Hq + 2 * Hkv) {"),
+    "cell_position_of_first_token": ("(double)positions[t], base, dst);", "(double)positions[0], base, dst);"),
 }
 
 

@@ -376,3 +376,62 @@ def test_oracle_matches_its_stored_regression_fixture():
     for key, qk in [("plain", False), ("qknorm", True)]:
         np.testing.assert_allclose(mod.compute(p, qk).reshape(-1), np.array(stored[key]),
                                    atol=1e-12, rtol=1e-12)
+
+
+# ------------------------------------- standalone q/k norm + RoPE cell ----
+
+def _norm_rope_case(T, Hq, Hkv, seed):
+    g = torch.Generator().manual_seed(seed)
+    qkv = torch.randn(T, (Hq + 2 * Hkv) * D, generator=g).to(torch.bfloat16)
+    qw = (1 + 0.1 * torch.randn(D, generator=g)).to(torch.bfloat16)
+    kw = (1 + 0.1 * torch.randn(D, generator=g)).to(torch.bfloat16)
+    pos = torch.randint(0, 1 << 20, (T,), generator=g, dtype=torch.int64)
+    return qkv, qw, kw, pos
+
+
+def _rotate(x, pos):
+    """NeoX rotation as a complex product: (x_j + i x_{j+32}) e^{i pos 10000^(-2j/64)}."""
+    j = np.arange(D // 2)
+    z = (x[..., :D // 2] + 1j * x[..., D // 2:]) * np.exp(1j * pos * 10000.0 ** (-2.0 * j / D))
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(6, 1), (24, 4)])
+def test_norm_rope_cell_matches_rms_norm_and_complex_rotation(Hq, Hkv):
+    T = 5
+    qkv, qw, kw, pos = _norm_rope_case(T, Hq, Hkv, 40 + Hq)
+    out = oracle.qk_norm_rope(qkv, pos, qw, kw, num_q_heads=Hq, num_kv_heads=Hkv)
+    x = qkv.double().view(T, Hq + 2 * Hkv, D)
+    for h in range(Hq + 2 * Hkv):
+        got = out[:, h * D:(h + 1) * D]
+        if h < Hq + Hkv:
+            w = (qw if h < Hq else kw).double()
+            n = torch.nn.functional.rms_norm(x[:, h], (D,), weight=w, eps=1e-5).numpy()
+            want = np.stack([_rotate(n[t], float(pos[t])) for t in range(T)])
+            # Angles reach 2^20 rad: fp64 rounding of pos * inv_freq alone
+            # moves sin/cos by ~2^20 * 2^-53.
+            np.testing.assert_allclose(got, want, rtol=1e-9, atol=1e-9)
+        else:  # value heads pass through exactly
+            assert np.array_equal(got, x[:, h].numpy())
+
+
+def test_norm_rope_cell_at_position_zero_is_the_norm_alone():
+    qkv, qw, kw, _ = _norm_rope_case(3, 6, 1, 7)
+    out = oracle.qk_norm_rope(qkv, torch.zeros(3, dtype=torch.int64), qw, kw, num_q_heads=6, num_kv_heads=1)
+    x = qkv.double().view(3, 8, D)
+    for h in range(7):
+        w = (qw if h < 6 else kw).double()
+        want = torch.nn.functional.rms_norm(x[:, h], (D,), weight=w, eps=1e-5).numpy()
+        np.testing.assert_allclose(out[:, h * D:(h + 1) * D], want, rtol=1e-13, atol=1e-13)
+
+
+def test_norm_rope_cell_scores_depend_on_relative_position():
+    # q of token 0 against k of token 1: shifting both positions by the same
+    # amount leaves the dot product unchanged (RoPE is a relative encoding).
+    qkv, qw, kw, _ = _norm_rope_case(2, 6, 1, 11)
+    dots = []
+    for shift in (0, 977, 123456):
+        out = oracle.qk_norm_rope(qkv, torch.tensor([5 + shift, 12 + shift]), qw, kw,
+                                  num_q_heads=6, num_kv_heads=1)
+        dots.append(float(out[0, 2 * D:3 * D] @ out[1, 6 * D:7 * D]))
+    assert max(dots) - min(dots) < 1e-9 * max(1.0, abs(dots[0]))

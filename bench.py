@@ -57,6 +57,11 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long_context")
+    ap.add_argument("--op", choices=["attn", "qk_norm_rope"], default="attn",
+                    help="attn: the block attention (headline); qk_norm_rope: the standalone "
+                         "fused q/k norm + RoPE call on --tokens tokens of --heads heads")
+    ap.add_argument("--tokens", type=int, default=64)
+    ap.add_argument("--heads", choices=["6/1", "24/4"], default="24/4")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -424,10 +429,78 @@ def run_ours(args, world, rank):
         print(json.dumps(line), flush=True)
 
 
+def run_norm_rope(args, world, rank):
+    """The standalone q/k norm + RoPE call: µs per call on T tokens, L2
+    flushed before each call; bytes = q and k heads read and written,
+    positions, weights."""
+    import speculative_decoding_drafter_k3_gb300 as k3da
+    from speculative_decoding_drafter_k3_gb300 import build as kbuild
+
+    kbuild.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    Hq, Hkv = (24, 4) if args.heads == "24/4" else (6, 1)
+    T, D = args.tokens, 64
+    g = torch.Generator().manual_seed(12)
+    qkv = torch.randn(T, (Hq + 2 * Hkv) * D, generator=g).to(torch.bfloat16).to(dev)
+    qw = (1 + 0.1 * torch.randn(D, generator=g)).to(torch.bfloat16).to(dev)
+    kw = (1 + 0.1 * torch.randn(D, generator=g)).to(torch.bfloat16).to(dev)
+    pos = torch.randint(0, 1 << 17, (T,), generator=g, dtype=torch.int64).to(dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def call():
+        k3da.k3da_qk_norm_rope(qkv, pos, qw, kw, num_q_heads=Hq, num_kv_heads=Hkv)
+
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    clocks = ClockSampler(dev.index) if rank == 0 else None
+    barrier(world)
+    for i in range(K):
+        flush_w.zero_()
+        ev[i][0].record()
+        call()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clock_info = clocks.stop() if clocks else None
+    ms = [e[0].elapsed_time(e[1]) for e in ev]
+    us = max_over_ranks(sum(ms), world) * 1e3 / (K * world)
+    nbytes = 2 * T * (Hq + Hkv) * D * 2 + T * 8 + 2 * D * 2
+    peak, peak_src = measured_hbm_peak()
+    achieved = nbytes / (us * 1e-6) / 1e9
+    # CPU baseline: the fp64 oracle of the cell on the same tokens.
+    import oracle
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < 2.0 or n < 3:
+        oracle.qk_norm_rope(qkv.cpu(), pos.cpu(), qw.cpu(), kw.cpu(), num_q_heads=Hq, num_kv_heads=Hkv)
+        n += 1
+    cpu_us = (time.perf_counter() - t0) / n * 1e6
+    line = {"metric": "fused q/k RMSNorm + NeoX RoPE µs/call", "value": us, "unit": "us/call",
+            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": us / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 math)",
+            "data": "synthetic (seeded N(0,1) bf16 qkv)",
+            "config": {"workload": f"qk_norm_rope_T{T}_{args.heads}", "tokens": T, "heads": args.heads,
+                       "head_dim": D, "positions": "int64",
+                       "l2": "flushed before every timed call (512 MB written)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "kernel": "k3da_norm_rope_kernel",
+                         "algorithmic_bytes_per_launch": nbytes, "launch_us": us, "peak_source": peak_src},
+            "e2e": None, "gpu_launches": K, "clocks": clock_info,
+            "cpu_baseline": {"value": cpu_us, "unit": "us/call", "cores": 1, "kind": "oracle",
+                             "sample": f"the whole call ({T} tokens), {n} runs"}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     world, rank = dist_setup(args)
-    if args.impl == "reference":
+    if args.op == "qk_norm_rope" and args.impl == "ours":
+        run_norm_rope(args, world, rank)
+    elif args.impl == "reference":
         run_reference(args, world, rank)
     else:
         run_ours(args, world, rank)

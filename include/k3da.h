@@ -183,6 +183,34 @@ size_t k3da_noalloc_scratch_bytes(void);
  */
 int k3da_split_grid(int device);
 
+/*
+ * k3da_qk_norm_rope -- the drafter's fused q/k RMSNorm + NeoX RoPE cell on
+ * its own (fused_qk_norm_rope in the commit adding the ops' contracts on the
+ * page "[None][feat] Share Kimi K3 FP4 modeling and add NVFP4 support on
+ * SM103"), in place: for every token t, each query head row of qkv becomes
+ * rope(rmsnorm(q, q_norm_w), positions[t]) and each key head row
+ * rope(rmsnorm(k, k_norm_w), positions[t]), rounded to bf16; value head rows
+ * are not touched.  RMSNorm is x * (mean(x^2) + eps)^(-1/2) * w over the 64
+ * dims of a head; RoPE turns the pairs (j, j+32) by positions[t] *
+ * rope_base^(-2j/64).  It is the transform k3da_attn_qknorm applies to the
+ * block's q and k before attending, exported for the step that writes new
+ * K into the pool.
+ *
+ *   qkv          [T, (Hq + 2*Hkv)*64] bf16, read and written.  2-byte aligned.
+ *   num_tokens   T >= 1 (the drafter runs 1..64).
+ *   num_q_heads, num_kv_heads   (6, 1) or (24, 4);  head_dim 64.
+ *   positions    [T] int32 or int64 (pos_dtype), aligned to its type.
+ *   q_norm_w, k_norm_w  [64] bf16, 2-byte aligned.
+ *   eps          finite, >= 0;  rope_base finite, > 1.
+ *   stream       cudaStream_t (NULL = legacy default stream).
+ *
+ * Returns K3DA_OK once the kernel is enqueued, else a k3da_error; nothing
+ * is written on a refusal.  Allocates nothing; graph-capturable.
+ */
+int k3da_qk_norm_rope(void *qkv, int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                      const void *positions, int pos_dtype, const void *q_norm_w,
+                      const void *k_norm_w, float eps, float rope_base, void *stream);
+
 /* Static description of a k3da_error or K3DA_STATUS_* bit set. */
 const char *k3da_error_string(int code);
 

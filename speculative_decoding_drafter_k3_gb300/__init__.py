@@ -37,7 +37,7 @@ STATUS_BAD_LENGTH, STATUS_BAD_PAGE, STATUS_TIMEOUT = 1, 2, 4
 POS_I32, POS_I64 = 0, 1
 EXPORTED = ["k3da_workspace_bytes", "k3da_attn", "k3da_attn_qknorm", "k3da_attn_qknorm_noalloc",
             "k3da_noalloc_scratch_bytes", "k3da_split_grid", "k3da_set_phase_event",
-            "k3da_error_string", "k3da_version"]
+            "k3da_error_string", "k3da_version", "k3da_qk_norm_rope"]
 
 
 class K3daError(ValueError):
@@ -80,6 +80,8 @@ def load_library():
         lib.k3da_set_phase_event.restype = c_int
         lib.k3da_version.argtypes = []
         lib.k3da_version.restype = c_int
+        lib.k3da_qk_norm_rope.argtypes = [vp, c_int, c_int, c_int, c_int, vp, c_int, vp, vp, c_f, c_f, vp]
+        lib.k3da_qk_norm_rope.restype = c_int
         _lib = lib
         return lib
 
@@ -173,6 +175,31 @@ def k3da_attn_qknorm(out, qkv, kv_pool, page_table, ctx_lens, positions, q_norm_
                               _stream(stream))
     _check(rc, "k3da_attn_qknorm")
     return out
+
+
+def k3da_qk_norm_rope(qkv, positions, q_norm_w, k_norm_w, *, num_q_heads: int, num_kv_heads: int,
+                      eps: float = 1e-5, rope_base: float = 10000.0, stream=None):
+    """The fused q/k RMSNorm + NeoX RoPE cell, in place on the q and k heads
+    of ``qkv`` ``[T, (Hq+2Hkv)*64]`` bf16 (C: k3da_qk_norm_rope)."""
+    lib = load_library()
+    for name, t in [("qkv", qkv), ("positions", positions), ("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)]:
+        if not t.is_cuda or not t.is_contiguous():
+            raise K3daError(f"{name} must be a contiguous CUDA tensor")
+    if qkv.dtype != torch.bfloat16 or qkv.dim() != 2:
+        raise K3daError("qkv must be [T, (Hq+2Hkv)*64] bf16")
+    D = qkv.shape[1] // (num_q_heads + 2 * num_kv_heads)
+    T = qkv.shape[0]
+    if positions.dtype not in (torch.int32, torch.int64) or positions.numel() != T:
+        raise K3daError("positions must be [T] int32 or int64")
+    if q_norm_w.dtype != torch.bfloat16 or k_norm_w.dtype != torch.bfloat16 or \
+            q_norm_w.numel() != D or k_norm_w.numel() != D:
+        raise K3daError("norm weights must be [head_dim] bf16")
+    pos_code = POS_I64 if positions.dtype == torch.int64 else POS_I32
+    rc = lib.k3da_qk_norm_rope(_ptr(qkv), T, num_q_heads, num_kv_heads, D, _ptr(positions), pos_code,
+                               _ptr(q_norm_w), _ptr(k_norm_w), float(eps), float(rope_base),
+                               _stream(stream))
+    _check(rc, "k3da_qk_norm_rope")
+    return qkv
 
 
 def alloc_workspace(num_requests: int, block_len: int, num_q_heads: int, num_kv_heads: int,

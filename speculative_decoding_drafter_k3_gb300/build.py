@@ -12,7 +12,7 @@ import sys
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", "k3da.cu")]
+SOURCES = [os.path.join(PKG, "csrc", "k3da.cu"), os.path.join(PKG, "csrc", "k3da_norm_rope.cu")]
 HEADERS = [os.path.join(ROOT, "include", "k3da.h")]
 LIB = os.path.join(PKG, "libk3da.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -135,3 +135,32 @@ def test_product_path_does_not_touch_the_oracle():
         if f.endswith((".py", ".c", ".h")):
             text = open(os.path.join(ROOT, "oracle", f)).read()
             assert "speculative_decoding_drafter_k3_gb300" not in text and "k3da.h" not in text, f
+
+
+def call_norm_rope(lib, **over):
+    a = dict(qkv=FAKE, T=64, Hq=6, Hkv=1, D=64, pos=FAKE, pos_dtype=k3da.POS_I64, qw=FAKE, kw=FAKE,
+             eps=1e-5, base=10000.0)
+    a.update(over)
+    return lib.k3da_qk_norm_rope(a["qkv"], a["T"], a["Hq"], a["Hkv"], a["D"], a["pos"], a["pos_dtype"],
+                                 a["qw"], a["kw"], a["eps"], a["base"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(qkv=None), k3da.EINVAL),
+    (dict(pos=None), k3da.EINVAL),
+    (dict(qw=None), k3da.EINVAL),
+    (dict(kw=None), k3da.EINVAL),
+    (dict(T=0), k3da.EINVAL),
+    (dict(Hq=8, Hkv=1), k3da.EUNSUPPORTED),
+    (dict(Hq=24, Hkv=1), k3da.EUNSUPPORTED),
+    (dict(D=128), k3da.EUNSUPPORTED),
+    (dict(pos_dtype=7), k3da.EINVAL),
+    (dict(pos=FAKE + 4), k3da.EINVAL),          # int64 positions on a 4-byte boundary
+    (dict(qkv=FAKE + 1), k3da.EINVAL),
+    (dict(eps=float("nan")), k3da.EINVAL),
+    (dict(eps=-1.0), k3da.EINVAL),
+    (dict(base=1.0), k3da.EINVAL),
+    (dict(base=float("inf")), k3da.EINVAL),
+])
+def test_norm_rope_refuses_out_of_contract_calls(lib, over, code):
+    assert call_norm_rope(lib, **over) == code

@@ -69,6 +69,22 @@ def _load():
                 ctypes.c_double, ctypes.c_double,
             ]
             lib.k3o_qk_norm_rope.restype = ctypes.c_int
+            d = ctypes.c_double
+            lib.k3o_yarn_inv_freq.argtypes = [dp, ctypes.c_int, d, d, d, d, d]
+            lib.k3o_yarn_inv_freq.restype = None
+            lib.k3o_rope_table.argtypes = [dp, ctypes.c_int, d, dp, d, dp]
+            lib.k3o_rope_table.restype = None
+            lib.k3o_attn_yarn.argtypes = [
+                vp, vp, vp, ctypes.c_int64, vp, ctypes.c_int, vp,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, d, vp, vp, vp, d, d, d, d, d, d, d,
+            ]
+            lib.k3o_attn_yarn.restype = ctypes.c_int
+            lib.k3o_qk_norm_rope_yarn.argtypes = [
+                vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp,
+                d, d, d, d, d, d, d,
+            ]
+            lib.k3o_qk_norm_rope_yarn.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -106,6 +122,31 @@ def rope_neox(x, pos: float, base: float = 10000.0) -> np.ndarray:
     return y
 
 
+def yarn_inv_freq(D: int, base: float, factor: float, original_max_position: float,
+                  beta_fast: float = 32.0, beta_slow: float = 1.0) -> np.ndarray:
+    """YaRN rotary frequencies of the D/2 pairs (fp64)."""
+    lib = _load()
+    inv = np.empty(D // 2, dtype=np.float64)
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.k3o_yarn_inv_freq(inv.ctypes.data_as(dp), D, float(base), float(factor),
+                          float(original_max_position), float(beta_slow), float(beta_fast))
+    return inv
+
+
+def rope_table(x, pos: float, inv_freq, mscale: float = 1.0) -> np.ndarray:
+    """Rotary embedding of one head row with an explicit frequency table,
+    both outputs scaled by ``mscale`` (fp64)."""
+    lib = _load()
+    x = _f64(x)
+    inv = _f64(inv_freq)
+    assert x.ndim == 1 and inv.shape[0] == x.shape[0] // 2
+    y = np.empty_like(x)
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.k3o_rope_table(x.ctypes.data_as(dp), x.shape[0], float(pos), inv.ctypes.data_as(dp),
+                       float(mscale), y.ctypes.data_as(dp))
+    return y
+
+
 def bf16_bits(a) -> np.ndarray:
     """uint16 bit patterns of a bf16 torch tensor, or a uint16 array as is."""
     if isinstance(a, np.ndarray):
@@ -121,7 +162,7 @@ def attn(qkv, pool, page_table, ctx_lens, *, num_requests: int, block_len: int,
          num_q_heads: int, num_kv_heads: int, head_dim: int = 64, page_size: int = 64,
          scale: float = 0.125, qknorm: bool = False, positions=None, q_norm_w=None,
          k_norm_w=None, eps: float = 1e-5, rope_base: float = 10000.0,
-         check: bool = True):
+         check: bool = True, yarn=None):
     """Drafter block attention in fp64; returns ``[T, Hq*D]`` float64.
 
     ``qkv``, ``pool``, ``q_norm_w`` and ``k_norm_w`` are bf16 (torch tensors or
@@ -152,9 +193,18 @@ def attn(qkv, pool, page_table, ctx_lens, *, num_requests: int, block_len: int,
     else:
         pos_p = qw_p = kw_p = None
     out = np.zeros((T, Hq * D), dtype=np.float64)
-    st = lib.k3o_attn(_ptr(out), _ptr(qkv_b), _ptr(pool_b), num_pages, _ptr(pt), pt.shape[1],
-                      _ptr(lens), R, B, Hq, Hkv, D, page_size, float(scale), int(bool(qknorm)),
-                      pos_p, qw_p, kw_p, float(eps), float(rope_base))
+    if yarn is not None:
+        # ``yarn``: dict(factor, original_max_position, beta_fast, beta_slow, mscale).
+        assert qknorm, "YaRN applies to the fused variant"
+        st = lib.k3o_attn_yarn(_ptr(out), _ptr(qkv_b), _ptr(pool_b), num_pages, _ptr(pt), pt.shape[1],
+                               _ptr(lens), R, B, Hq, Hkv, D, page_size, float(scale), pos_p, qw_p, kw_p,
+                               float(eps), float(rope_base), float(yarn["factor"]),
+                               float(yarn["original_max_position"]), float(yarn["beta_fast"]),
+                               float(yarn["beta_slow"]), float(yarn["mscale"]))
+    else:
+        st = lib.k3o_attn(_ptr(out), _ptr(qkv_b), _ptr(pool_b), num_pages, _ptr(pt), pt.shape[1],
+                          _ptr(lens), R, B, Hq, Hkv, D, page_size, float(scale), int(bool(qknorm)),
+                          pos_p, qw_p, kw_p, float(eps), float(rope_base))
     if check:
         if st != OK:
             raise ValueError(f"oracle refused the inputs (status {st})")
@@ -163,7 +213,8 @@ def attn(qkv, pool, page_table, ctx_lens, *, num_requests: int, block_len: int,
 
 
 def qk_norm_rope(qkv, positions, q_norm_w, k_norm_w, *, num_q_heads: int, num_kv_heads: int,
-                 head_dim: int = 64, eps: float = 1e-5, rope_base: float = 10000.0) -> np.ndarray:
+                 head_dim: int = 64, eps: float = 1e-5, rope_base: float = 10000.0,
+                 yarn=None) -> np.ndarray:
     """The fused q/k norm + RoPE cell in fp64: ``[T, (Hq+2Hkv)*D]`` float64
     with q and k heads normalised and rotated at their token's position and
     v heads copied.  ``qkv``, ``q_norm_w``, ``k_norm_w`` are bf16; positions
@@ -180,8 +231,14 @@ def qk_norm_rope(qkv, positions, q_norm_w, k_norm_w, *, num_q_heads: int, num_kv
     kw = bf16_bits(k_norm_w).reshape(-1)
     assert qw.shape[0] == D and kw.shape[0] == D
     out = np.zeros((T, W), dtype=np.float64)
-    st = lib.k3o_qk_norm_rope(_ptr(out), _ptr(qkv_b), T, Hq, Hkv, D, _ptr(pos), _ptr(qw), _ptr(kw),
-                              float(eps), float(rope_base))
+    if yarn is not None:
+        st = lib.k3o_qk_norm_rope_yarn(_ptr(out), _ptr(qkv_b), T, Hq, Hkv, D, _ptr(pos), _ptr(qw), _ptr(kw),
+                                       float(eps), float(rope_base), float(yarn["factor"]),
+                                       float(yarn["original_max_position"]), float(yarn["beta_fast"]),
+                                       float(yarn["beta_slow"]), float(yarn["mscale"]))
+    else:
+        st = lib.k3o_qk_norm_rope(_ptr(out), _ptr(qkv_b), T, Hq, Hkv, D, _ptr(pos), _ptr(qw), _ptr(kw),
+                                  float(eps), float(rope_base))
     if st != OK:
         raise ValueError(f"oracle refused the inputs (status {st})")
     return out

@@ -80,6 +80,58 @@ void k3o_rope_neox(const double *x, int D, double pos, double base, double *y)
     free(tmp);
 }
 
+/*
+ * YaRN frequencies ("YaRN: Efficient Context Window Extension of Large
+ * Language Models", Peng et al. 2023, the "NTK-by-parts" interpolation with
+ * its ramp): pair j of the plain table turns at theta_j = base^(-2j/D), with
+ * wavelength lambda_j = 2 pi / theta_j, and sees r_j = orig_len / lambda_j
+ * wavelengths in the original context.  gamma = 0 below r = alpha, 1 above
+ * r = beta, linear in between; the new frequency is
+ * (1 - gamma) * theta_j / factor + gamma * theta_j.  factor 1 is the plain
+ * table.
+ */
+void k3o_yarn_inv_freq(double *inv_freq, int D, double base, double factor, double orig_len,
+                       double alpha, double beta)
+{
+    const double two_pi = 6.283185307179586476925286766559;
+    for (int j = 0; j < D / 2; ++j) {
+        double theta = pow(base, -2.0 * (double)j / (double)D);
+        if (factor == 1.0) {
+            inv_freq[j] = theta;
+            continue;
+        }
+        double wavelength = two_pi / theta;
+        double r = orig_len / wavelength;
+        double gamma;
+        if (r < alpha)
+            gamma = 0.0;
+        else if (r > beta)
+            gamma = 1.0;
+        else
+            gamma = (r - alpha) / (beta - alpha);
+        inv_freq[j] = (1.0 - gamma) * theta / factor + gamma * theta;
+    }
+}
+
+/* Rotary embedding of one head row with an explicit frequency table: pair
+ * (j, j + D/2) turns by pos * inv_freq[j]; both outputs are multiplied by
+ * mscale (YaRN's attention temperature, sqrt(1/t), applied to q and k). */
+void k3o_rope_table(const double *x, int D, double pos, const double *inv_freq, double mscale,
+                    double *y)
+{
+    int half = D / 2;
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int j = 0; j < half; ++j) {
+        double theta = pos * inv_freq[j];
+        double c = cos(theta), s = sin(theta);
+        double lo = x[j], hi = x[j + half];
+        tmp[j] = (lo * c - hi * s) * mscale;
+        tmp[j + half] = (hi * c + lo * s) * mscale;
+    }
+    memcpy(y, tmp, sizeof(double) * (size_t)D);
+    free(tmp);
+}
+
 /* Error codes of k3o_attn. */
 enum {
     K3O_OK = 0,
@@ -104,11 +156,12 @@ enum {
  * Returns K3O_OK, or an error code without a meaningful output when a length
  * or a page id that would be read is out of range.
  */
-int k3o_attn(double *out, const uint16_t *qkv, const uint16_t *pool,
-             int64_t num_pages, const int32_t *page_table, int page_stride,
-             const int32_t *ctx_lens, int R, int B, int Hq, int Hkv, int D,
-             int page_size, double scale, int qknorm, const int64_t *positions,
-             const uint16_t *q_w, const uint16_t *k_w, double eps, double base)
+static int attn_core(double *out, const uint16_t *qkv, const uint16_t *pool,
+                     int64_t num_pages, const int32_t *page_table, int page_stride,
+                     const int32_t *ctx_lens, int R, int B, int Hq, int Hkv, int D,
+                     int page_size, double scale, int qknorm, const int64_t *positions,
+                     const uint16_t *q_w, const uint16_t *k_w, double eps, double base,
+                     const double *inv_freq, double mscale)
 {
     if (R < 1 || B < 1 || Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || D < 2 ||
         D % 2 != 0 || page_size < 1 || page_stride < 1)
@@ -176,7 +229,10 @@ int k3o_attn(double *out, const uint16_t *qkv, const uint16_t *pool,
                 double *kdst = K + (L + jb) * D;
                 if (qknorm) {
                     k3o_rmsnorm(raw, wk, D, eps, tmp);
-                    k3o_rope_neox(tmp, D, (double)positions[t], base, kdst);
+                    if (inv_freq)
+                        k3o_rope_table(tmp, D, (double)positions[t], inv_freq, mscale, kdst);
+                    else
+                        k3o_rope_neox(tmp, D, (double)positions[t], base, kdst);
                 } else {
                     memcpy(kdst, raw, sizeof(double) * (size_t)D);
                 }
@@ -193,7 +249,10 @@ int k3o_attn(double *out, const uint16_t *qkv, const uint16_t *pool,
                         raw[j] = bf16_bits_to_f64(qr[j]);
                     if (qknorm) {
                         k3o_rmsnorm(raw, wq, D, eps, tmp);
-                        k3o_rope_neox(tmp, D, (double)positions[t], base, q);
+                        if (inv_freq)
+                            k3o_rope_table(tmp, D, (double)positions[t], inv_freq, mscale, q);
+                        else
+                            k3o_rope_neox(tmp, D, (double)positions[t], base, q);
                     } else {
                         memcpy(q, raw, sizeof(double) * (size_t)D);
                     }
@@ -227,6 +286,42 @@ int k3o_attn(double *out, const uint16_t *qkv, const uint16_t *pool,
     return status;
 }
 
+int k3o_attn(double *out, const uint16_t *qkv, const uint16_t *pool,
+             int64_t num_pages, const int32_t *page_table, int page_stride,
+             const int32_t *ctx_lens, int R, int B, int Hq, int Hkv, int D,
+             int page_size, double scale, int qknorm, const int64_t *positions,
+             const uint16_t *q_w, const uint16_t *k_w, double eps, double base)
+{
+    return attn_core(out, qkv, pool, num_pages, page_table, page_stride, ctx_lens, R, B, Hq, Hkv,
+                     D, page_size, scale, qknorm, positions, q_w, k_w, eps, base, NULL, 1.0);
+}
+
+/*
+ * The fused variant with YaRN RoPE: as k3o_attn with qknorm = 1, but the
+ * block's q and k turn by the YaRN frequencies of k3o_yarn_inv_freq
+ * (factor, orig_len, alpha = beta_slow, beta = beta_fast) and are scaled by
+ * mscale.  factor 1 and mscale 1 give k3o_attn's fused result.
+ */
+int k3o_attn_yarn(double *out, const uint16_t *qkv, const uint16_t *pool,
+                  int64_t num_pages, const int32_t *page_table, int page_stride,
+                  const int32_t *ctx_lens, int R, int B, int Hq, int Hkv, int D,
+                  int page_size, double scale, const int64_t *positions,
+                  const uint16_t *q_w, const uint16_t *k_w, double eps, double base,
+                  double factor, double orig_len, double beta_fast, double beta_slow,
+                  double mscale)
+{
+    if (D < 2 || D % 2 != 0)
+        return K3O_BAD_SHAPE;
+    double *inv = (double *)malloc(sizeof(double) * (size_t)(D / 2));
+    if (!inv)
+        return K3O_NO_MEMORY;
+    k3o_yarn_inv_freq(inv, D, base, factor, orig_len, beta_slow, beta_fast);
+    int st = attn_core(out, qkv, pool, num_pages, page_table, page_stride, ctx_lens, R, B, Hq, Hkv,
+                       D, page_size, scale, 1, positions, q_w, k_w, eps, base, inv, mscale);
+    free(inv);
+    return st;
+}
+
 /*
  * The drafter's fused q/k norm + RoPE cell on its own (the fused_qk_norm_rope
  * cell of the commit adding the ops' contracts), for T tokens of qkv:
@@ -240,9 +335,9 @@ int k3o_attn(double *out, const uint16_t *qkv, const uint16_t *pool,
  *
  * Returns K3O_OK, K3O_BAD_SHAPE or K3O_NO_MEMORY.
  */
-int k3o_qk_norm_rope(double *out, const uint16_t *qkv, int T, int Hq, int Hkv, int D,
-                     const int64_t *positions, const uint16_t *q_w, const uint16_t *k_w,
-                     double eps, double base)
+static int norm_rope_core(double *out, const uint16_t *qkv, int T, int Hq, int Hkv, int D,
+                          const int64_t *positions, const uint16_t *q_w, const uint16_t *k_w,
+                          double eps, double base, const double *inv_freq, double mscale)
 {
     if (T < 1 || Hq < 1 || Hkv < 1 || D < 2 || (D % 2) != 0)
         return K3O_BAD_SHAPE;
@@ -267,7 +362,10 @@ int k3o_qk_norm_rope(double *out, const uint16_t *qkv, int T, int Hq, int Hkv, i
                 raw[j] = bf16_bits_to_f64(src[j]);
             if (h < Hq + Hkv) {
                 k3o_rmsnorm(raw, h < Hq ? wq : wk, D, eps, tmp);
-                k3o_rope_neox(tmp, D, (double)positions[t], base, dst);
+                if (inv_freq)
+                    k3o_rope_table(tmp, D, (double)positions[t], inv_freq, mscale, dst);
+                else
+                    k3o_rope_neox(tmp, D, (double)positions[t], base, dst);
             } else {
                 memcpy(dst, raw, sizeof(double) * (size_t)D);
             }
@@ -275,4 +373,28 @@ int k3o_qk_norm_rope(double *out, const uint16_t *qkv, int T, int Hq, int Hkv, i
     }
     free(wq); free(wk); free(raw); free(tmp);
     return K3O_OK;
+}
+
+int k3o_qk_norm_rope(double *out, const uint16_t *qkv, int T, int Hq, int Hkv, int D,
+                     const int64_t *positions, const uint16_t *q_w, const uint16_t *k_w,
+                     double eps, double base)
+{
+    return norm_rope_core(out, qkv, T, Hq, Hkv, D, positions, q_w, k_w, eps, base, NULL, 1.0);
+}
+
+/* The cell with YaRN RoPE (see k3o_attn_yarn). */
+int k3o_qk_norm_rope_yarn(double *out, const uint16_t *qkv, int T, int Hq, int Hkv, int D,
+                          const int64_t *positions, const uint16_t *q_w, const uint16_t *k_w,
+                          double eps, double base, double factor, double orig_len,
+                          double beta_fast, double beta_slow, double mscale)
+{
+    if (D < 2 || D % 2 != 0)
+        return K3O_BAD_SHAPE;
+    double *inv = (double *)malloc(sizeof(double) * (size_t)(D / 2));
+    if (!inv)
+        return K3O_NO_MEMORY;
+    k3o_yarn_inv_freq(inv, D, base, factor, orig_len, beta_slow, beta_fast);
+    int st = norm_rope_core(out, qkv, T, Hq, Hkv, D, positions, q_w, k_w, eps, base, inv, mscale);
+    free(inv);
+    return st;
 }

@@ -12,9 +12,11 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 # name -> (text in the oracle, the planted mistake)
 MUTANTS = {
-    "rope_frequency_exponent": ("-2.0 * (double)j / (double)D", "-1.0 * (double)j / (double)D"),
+    "rope_frequency_exponent": ("double inv_freq = pow(base, -2.0 * (double)j / (double)D);",
+                                "double inv_freq = pow(base, -1.0 * (double)j / (double)D);"),
     "rope_rotation_sign": ("tmp[j] = lo * c - hi * s;", "tmp[j] = lo * c + hi * s;"),
-    "rope_interleaved_pairs": ("double lo = x[j], hi = x[j + half];", "double lo = x[j], hi = x[(j + 1) % D];"),
+    "rope_interleaved_pairs": ("double lo = x[j], hi = x[j + half];\n        tmp[j] = lo * c - hi * s;",
+                               "double lo = x[j], hi = x[(j + 1) % D];\n        tmp[j] = lo * c - hi * s;"),
     "gqa_head_modulo": ("const int h = g * G + hl;", "const int h = hl * Hkv + g;"),
     "softmax_scale_dropped": ("s[k] = scale * dot;", "s[k] = dot;"),
     "page_slot_off_by_one": ("int64_t slot = c % page_size;", "int64_t slot = (c + 1) % page_size;"),
@@ -31,6 +33,11 @@ MUTANTS = {
                                    "k3o_rmsnorm(raw, wq, D, eps, tmp);"),
     "cell_v_heads_normalised": ("if (h < Hq + Hkv) {", "if (h < Hq + 2 * Hkv) {"),
     "cell_position_of_first_token": ("(double)positions[t], base, dst);", "(double)positions[0], base, dst);"),
+    "yarn_ramp_inverted": ("inv_freq[j] = (1.0 - gamma) * theta / factor + gamma * theta;",
+                           "inv_freq[j] = gamma * theta / factor + (1.0 - gamma) * theta;"),
+    "yarn_wavelength_without_two_pi": ("double wavelength = two_pi / theta;", "double wavelength = 1.0 / theta;"),
+    "yarn_mscale_on_one_output": ("tmp[j + half] = (hi * c + lo * s) * mscale;",
+                                  "tmp[j + half] = (hi * c + lo * s);"),
 }
 
 

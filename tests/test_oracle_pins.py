@@ -435,3 +435,117 @@ def test_norm_rope_cell_scores_depend_on_relative_position():
                                   num_q_heads=6, num_kv_heads=1)
         dots.append(float(out[0, 2 * D:3 * D] @ out[1, 6 * D:7 * D]))
     assert max(dots) - min(dots) < 1e-9 * max(1.0, abs(dots[0]))
+
+
+# ----------------------------------------------------------------- YaRN ----
+# The pages name YaRN with factor 4.0 for the drafter; the method is the
+# "NTK-by-parts" interpolation of the YaRN paper (Peng et al. 2023): pairs
+# with many wavelengths in the original context keep their frequency, pairs
+# with less than one are slowed by the factor, a linear ramp in between, and
+# q and k are scaled by mscale.
+
+def _plain_inv(D=64, base=10000.0):
+    return base ** (-2.0 * np.arange(D // 2) / D)
+
+
+def test_yarn_factor_one_is_the_plain_table():
+    np.testing.assert_allclose(oracle.yarn_inv_freq(64, 10000.0, 1.0, 4096.0), _plain_inv(), rtol=1e-15)
+
+
+def test_yarn_keeps_fast_pairs_and_slows_slow_pairs_by_the_factor():
+    inv0 = _plain_inv()
+    r = 4096.0 * inv0 / (2 * math.pi)  # wavelengths of each pair inside 4096 positions
+    inv = oracle.yarn_inv_freq(64, 10000.0, 4.0, 4096.0, beta_fast=32.0, beta_slow=1.0)
+    fast, slow = r > 32.0, r < 1.0
+    assert fast.any() and slow.any() and (~fast & ~slow).any()
+    np.testing.assert_allclose(inv[fast], inv0[fast], rtol=1e-15)
+    np.testing.assert_allclose(inv[slow], inv0[slow] / 4.0, rtol=1e-15)
+    mid = ~fast & ~slow
+    assert (inv[mid] < inv0[mid]).all() and (inv[mid] > inv0[mid] / 4.0).all()
+    # Frequencies stay in decreasing order through the ramp.
+    assert (np.diff(inv) < 0).all()
+
+
+def test_yarn_ramp_midpoint_closed_form():
+    # Put pair 10 exactly halfway up the ramp (r = (1 + 32) / 2): it turns at
+    # theta * ((1 - 1/2) / 4 + 1/2) = 0.625 theta.
+    theta = 10000.0 ** (-20.0 / 64)
+    orig = 16.5 * 2 * math.pi / theta
+    inv = oracle.yarn_inv_freq(64, 10000.0, 4.0, orig, beta_fast=32.0, beta_slow=1.0)
+    assert abs(inv[10] / theta - 0.625) < 1e-13
+
+
+def test_yarn_with_every_pair_slowed_is_rope_at_a_scaled_position():
+    g = np.random.default_rng(3)
+    x = g.standard_normal(64)
+    inv = oracle.yarn_inv_freq(64, 10000.0, 4.0, 1e-3)  # no pair completes a wavelength: all slowed
+    np.testing.assert_allclose(inv, _plain_inv() / 4.0, rtol=1e-15)
+    for pos in (0, 4, 4 * 977, 4 * 123457):
+        np.testing.assert_allclose(oracle.rope_table(x, pos, inv), oracle.rope_neox(x, pos // 4), rtol=1e-12,
+                                   atol=1e-12)
+
+
+def test_rope_table_scales_every_pair_norm_by_mscale():
+    g = np.random.default_rng(4)
+    x = g.standard_normal(64)
+    y = oracle.rope_table(x, 12345.0, _plain_inv(), mscale=1.3862943611198906)
+    n_in = np.hypot(x[:32], x[32:])
+    n_out = np.hypot(y[:32], y[32:])
+    np.testing.assert_allclose(n_out, 1.3862943611198906 * n_in, rtol=1e-13)
+
+
+def _attn_case(seed):
+    g = torch.Generator().manual_seed(seed)
+    R, B, Hq, Hkv, S = 2, 3, 6, 1, 3
+    qkv = torch.randn(R * B, (Hq + 2 * Hkv) * D, generator=g).to(torch.bfloat16)
+    pool = torch.randn(6, 2, Hkv, P, D, generator=g).to(torch.bfloat16)
+    pt = torch.tensor([[4, 1, 0], [2, 5, 3]], dtype=torch.int32)
+    lens = torch.tensor([130, 70], dtype=torch.int32)
+    qw = (1 + 0.1 * torch.randn(D, generator=g)).to(torch.bfloat16)
+    kw = (1 + 0.1 * torch.randn(D, generator=g)).to(torch.bfloat16)
+    return dict(qkv=qkv, pool=pool, page_table=pt, ctx_lens=lens, num_requests=R, block_len=B,
+                num_q_heads=Hq, num_kv_heads=Hkv, qknorm=True, q_norm_w=qw, k_norm_w=kw)
+
+
+def test_attention_with_yarn_factor_one_is_the_fused_variant():
+    c = _attn_case(21)
+    pos = torch.tensor([130, 131, 132, 70, 71, 72])
+    plain = oracle.attn(positions=pos, **c)
+    yarn = oracle.attn(positions=pos, yarn=dict(factor=1.0, original_max_position=4096.0, beta_fast=32.0,
+                                                beta_slow=1.0, mscale=1.0), **c)
+    np.testing.assert_allclose(yarn, plain, rtol=1e-14, atol=1e-14)
+
+
+def test_attention_with_every_pair_slowed_and_mscale_closed_form():
+    # All pairs slowed by 4 and q, k scaled by m: with block keys only (the
+    # pool's context keys are used as stored, unscaled) the scores are those
+    # of the plain fused variant at positions / 4 with the scale times m^2.
+    c = _attn_case(22)
+    c["ctx_lens"] = torch.zeros(2, dtype=torch.int32)
+    pos = torch.tensor([4 * 130, 4 * 131, 4 * 132, 4 * 70, 4 * 71, 4 * 72])
+    m = 0.1 * math.log(4.0) + 1.0
+    yarn = oracle.attn(positions=pos, yarn=dict(factor=4.0, original_max_position=1e-3, beta_fast=32.0,
+                                                beta_slow=1.0, mscale=m), **c)
+    plain = oracle.attn(positions=pos // 4, scale=0.125 * m * m, **c)
+    np.testing.assert_allclose(yarn, plain, rtol=1e-11, atol=1e-12)
+
+
+def test_norm_rope_cell_with_yarn_factor_one_is_the_plain_cell():
+    qkv, qw, kw, pos = _norm_rope_case(4, 24, 4, 13)
+    plain = oracle.qk_norm_rope(qkv, pos, qw, kw, num_q_heads=24, num_kv_heads=4)
+    yarn = oracle.qk_norm_rope(qkv, pos, qw, kw, num_q_heads=24, num_kv_heads=4,
+                               yarn=dict(factor=1.0, original_max_position=4096.0, beta_fast=32.0,
+                                         beta_slow=1.0, mscale=1.0))
+    np.testing.assert_allclose(yarn, plain, rtol=1e-14, atol=1e-14)
+
+
+def test_norm_rope_cell_with_every_pair_slowed_closed_form():
+    qkv, qw, kw, pos = _norm_rope_case(4, 6, 1, 14)
+    m = 1.1386294361119891
+    yarn = oracle.qk_norm_rope(qkv, 4 * pos, qw, kw, num_q_heads=6, num_kv_heads=1,
+                               yarn=dict(factor=4.0, original_max_position=1e-3, beta_fast=32.0,
+                                         beta_slow=1.0, mscale=m))
+    plain = oracle.qk_norm_rope(qkv, pos, qw, kw, num_q_heads=6, num_kv_heads=1)
+    qk = 7 * D  # q and k heads scale by m; v heads pass through
+    np.testing.assert_allclose(yarn[:, :qk], m * plain[:, :qk], rtol=1e-11, atol=1e-11)
+    assert np.array_equal(yarn[:, qk:], plain[:, qk:])

@@ -184,6 +184,41 @@ size_t k3da_noalloc_scratch_bytes(void);
 int k3da_split_grid(int device);
 
 /*
+ * YaRN RoPE scaling (next to "YaRN 4.0", the drafter's setting on the page
+ * cited above; the method is the "NTK-by-parts" interpolation of "YaRN:
+ * Efficient Context Window Extension of Large Language Models", Peng et al.
+ * 2023).  Pair j of the plain table turns at theta_j = rope_base^(-2j/64);
+ * with r_j = original_max_position * theta_j / (2 pi) (its wavelengths in the
+ * original context) and the ramp g = clamp((r_j - beta_slow) / (beta_fast -
+ * beta_slow), 0, 1), it turns at g * theta_j + (1 - g) * theta_j / factor.
+ * Both rotated outputs are multiplied by mscale (the paper's sqrt(1/t), i.e.
+ * 0.1 * ln(factor) + 1, applied to q and k; pass 1 when the model folds it
+ * elsewhere).  factor 1 with mscale 1 is plain NeoX RoPE.  Host memory; read
+ * during the call only.
+ */
+typedef struct {
+    float factor;                /* >= 1 */
+    float original_max_position; /* > 0 */
+    float beta_fast;             /* > beta_slow (32 in the paper) */
+    float beta_slow;             /* > 0 (1 in the paper) */
+    float mscale;                /* > 0 */
+} k3da_yarn;
+
+/*
+ * k3da_attn_qknorm_yarn -- k3da_attn_qknorm with the block's q and k rotated
+ * by YaRN RoPE (`yarn`, see k3da_yarn) instead of plain NeoX RoPE; every
+ * other argument, the workspace contract and the errors are those of
+ * k3da_attn_qknorm.  K3DA_EINVAL when `yarn` is NULL or out of range.
+ */
+int k3da_attn_qknorm_yarn(void *out, const void *qkv, const void *kv_pool, int64_t num_pages,
+                          const int32_t *page_table, int page_stride, const int32_t *ctx_lens,
+                          int num_requests, int block_len, int num_q_heads, int num_kv_heads,
+                          int head_dim, float softmax_scale, const void *positions, int pos_dtype,
+                          const void *q_norm_w, const void *k_norm_w, float eps, float rope_base,
+                          const k3da_yarn *yarn, void *workspace, size_t workspace_bytes,
+                          int32_t *status, void *stream);
+
+/*
  * k3da_qk_norm_rope -- the drafter's fused q/k RMSNorm + NeoX RoPE cell on
  * its own (fused_qk_norm_rope in the commit adding the ops' contracts on the
  * page "[None][feat] Share Kimi K3 FP4 modeling and add NVFP4 support on
@@ -210,6 +245,12 @@ int k3da_split_grid(int device);
 int k3da_qk_norm_rope(void *qkv, int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
                       const void *positions, int pos_dtype, const void *q_norm_w,
                       const void *k_norm_w, float eps, float rope_base, void *stream);
+
+/* k3da_qk_norm_rope with YaRN RoPE (`yarn`, see k3da_yarn). */
+int k3da_qk_norm_rope_yarn(void *qkv, int num_tokens, int num_q_heads, int num_kv_heads,
+                           int head_dim, const void *positions, int pos_dtype,
+                           const void *q_norm_w, const void *k_norm_w, float eps, float rope_base,
+                           const k3da_yarn *yarn, void *stream);
 
 /* Static description of a k3da_error or K3DA_STATUS_* bit set. */
 const char *k3da_error_string(int code);

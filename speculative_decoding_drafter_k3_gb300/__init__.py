@@ -37,7 +37,26 @@ STATUS_BAD_LENGTH, STATUS_BAD_PAGE, STATUS_TIMEOUT = 1, 2, 4
 POS_I32, POS_I64 = 0, 1
 EXPORTED = ["k3da_workspace_bytes", "k3da_attn", "k3da_attn_qknorm", "k3da_attn_qknorm_noalloc",
             "k3da_noalloc_scratch_bytes", "k3da_split_grid", "k3da_set_phase_event",
-            "k3da_error_string", "k3da_version", "k3da_qk_norm_rope"]
+            "k3da_error_string", "k3da_version", "k3da_qk_norm_rope", "k3da_attn_qknorm_yarn",
+            "k3da_qk_norm_rope_yarn"]
+
+
+class Yarn(ctypes.Structure):
+    """k3da_yarn: YaRN RoPE scaling (factor, original_max_position, beta_fast,
+    beta_slow, mscale); mscale = 0.1 ln(factor) + 1 in the YaRN paper."""
+    _fields_ = [("factor", ctypes.c_float), ("original_max_position", ctypes.c_float),
+                ("beta_fast", ctypes.c_float), ("beta_slow", ctypes.c_float), ("mscale", ctypes.c_float)]
+
+    @classmethod
+    def of(cls, factor: float, original_max_position: float, beta_fast: float = 32.0,
+           beta_slow: float = 1.0, mscale=None):
+        if mscale is None:
+            import math
+            mscale = 0.1 * math.log(factor) + 1.0
+        return cls(factor, original_max_position, beta_fast, beta_slow, mscale)
+
+    def as_dict(self):
+        return {k: float(getattr(self, k)) for k, _ in self._fields_}
 
 
 class K3daError(ValueError):
@@ -82,6 +101,11 @@ def load_library():
         lib.k3da_version.restype = c_int
         lib.k3da_qk_norm_rope.argtypes = [vp, c_int, c_int, c_int, c_int, vp, c_int, vp, vp, c_f, c_f, vp]
         lib.k3da_qk_norm_rope.restype = c_int
+        yp = ctypes.POINTER(Yarn)
+        lib.k3da_attn_qknorm_yarn.argtypes = common + [vp, c_int, vp, vp, c_f, c_f, yp, vp, c_sz, vp, vp]
+        lib.k3da_attn_qknorm_yarn.restype = c_int
+        lib.k3da_qk_norm_rope_yarn.argtypes = [vp, c_int, c_int, c_int, c_int, vp, c_int, vp, vp, c_f, c_f, yp, vp]
+        lib.k3da_qk_norm_rope_yarn.restype = c_int
         _lib = lib
         return lib
 
@@ -153,8 +177,9 @@ def k3da_attn(out, qkv, kv_pool, page_table, ctx_lens, *, block_len: int, num_q_
 def k3da_attn_qknorm(out, qkv, kv_pool, page_table, ctx_lens, positions, q_norm_w, k_norm_w, *,
                      block_len: int, num_q_heads: int, num_kv_heads: int,
                      softmax_scale: float = 0.125, eps: float = 1e-5, rope_base: float = 10000.0,
-                     workspace, status=None, stream=None):
-    """Block attention with fused q/k RMSNorm + NeoX RoPE (C: k3da_attn_qknorm)."""
+                     workspace, status=None, stream=None, yarn=None):
+    """Block attention with fused q/k RMSNorm + NeoX RoPE (C: k3da_attn_qknorm);
+    with ``yarn`` (a ``Yarn``), YaRN RoPE (C: k3da_attn_qknorm_yarn)."""
     lib = load_library()
     R, num_pages, S, D = _shape_args(out, qkv, kv_pool, page_table, ctx_lens, block_len,
                                      num_q_heads, num_kv_heads)
@@ -167,20 +192,24 @@ def k3da_attn_qknorm(out, qkv, kv_pool, page_table, ctx_lens, positions, q_norm_
             q_norm_w.numel() != D or k_norm_w.numel() != D:
         raise K3daError("norm weights must be [64] bf16")
     pos_code = POS_I64 if positions.dtype == torch.int64 else POS_I32
-    rc = lib.k3da_attn_qknorm(_ptr(out), _ptr(qkv), _ptr(kv_pool), num_pages, _ptr(page_table), S,
-                              _ptr(ctx_lens), R, block_len, num_q_heads, num_kv_heads, D,
-                              float(softmax_scale), _ptr(positions), pos_code, _ptr(q_norm_w),
-                              _ptr(k_norm_w), float(eps), float(rope_base), _ptr(workspace),
-                              workspace.numel() * workspace.element_size(), _ptr(status),
-                              _stream(stream))
-    _check(rc, "k3da_attn_qknorm")
+    args = [_ptr(out), _ptr(qkv), _ptr(kv_pool), num_pages, _ptr(page_table), S, _ptr(ctx_lens), R,
+            block_len, num_q_heads, num_kv_heads, D, float(softmax_scale), _ptr(positions), pos_code,
+            _ptr(q_norm_w), _ptr(k_norm_w), float(eps), float(rope_base)]
+    tail = [_ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)]
+    if yarn is None:
+        rc = lib.k3da_attn_qknorm(*args, *tail)
+        _check(rc, "k3da_attn_qknorm")
+    else:
+        rc = lib.k3da_attn_qknorm_yarn(*args, ctypes.byref(yarn), *tail)
+        _check(rc, "k3da_attn_qknorm_yarn")
     return out
 
 
 def k3da_qk_norm_rope(qkv, positions, q_norm_w, k_norm_w, *, num_q_heads: int, num_kv_heads: int,
-                      eps: float = 1e-5, rope_base: float = 10000.0, stream=None):
+                      eps: float = 1e-5, rope_base: float = 10000.0, stream=None, yarn=None):
     """The fused q/k RMSNorm + NeoX RoPE cell, in place on the q and k heads
-    of ``qkv`` ``[T, (Hq+2Hkv)*64]`` bf16 (C: k3da_qk_norm_rope)."""
+    of ``qkv`` ``[T, (Hq+2Hkv)*64]`` bf16 (C: k3da_qk_norm_rope); with
+    ``yarn`` (a ``Yarn``), YaRN RoPE (C: k3da_qk_norm_rope_yarn)."""
     lib = load_library()
     for name, t in [("qkv", qkv), ("positions", positions), ("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)]:
         if not t.is_cuda or not t.is_contiguous():
@@ -195,10 +224,14 @@ def k3da_qk_norm_rope(qkv, positions, q_norm_w, k_norm_w, *, num_q_heads: int, n
             q_norm_w.numel() != D or k_norm_w.numel() != D:
         raise K3daError("norm weights must be [head_dim] bf16")
     pos_code = POS_I64 if positions.dtype == torch.int64 else POS_I32
-    rc = lib.k3da_qk_norm_rope(_ptr(qkv), T, num_q_heads, num_kv_heads, D, _ptr(positions), pos_code,
-                               _ptr(q_norm_w), _ptr(k_norm_w), float(eps), float(rope_base),
-                               _stream(stream))
-    _check(rc, "k3da_qk_norm_rope")
+    args = [_ptr(qkv), T, num_q_heads, num_kv_heads, D, _ptr(positions), pos_code, _ptr(q_norm_w),
+            _ptr(k_norm_w), float(eps), float(rope_base)]
+    if yarn is None:
+        rc = lib.k3da_qk_norm_rope(*args, _stream(stream))
+        _check(rc, "k3da_qk_norm_rope")
+    else:
+        rc = lib.k3da_qk_norm_rope_yarn(*args, ctypes.byref(yarn), _stream(stream))
+        _check(rc, "k3da_qk_norm_rope_yarn")
     return qkv
 
 
@@ -214,8 +247,9 @@ def case_workspace(case) -> torch.Tensor:
     return alloc_workspace(case.R, case.B, case.Hq, case.Hkv, case.page_stride, case.qkv.device)
 
 
-def run_case(case, out=None, workspace=None, status=None, stream=None):
-    """Run the op on a ``workloads.Case`` whose tensors are on the GPU."""
+def run_case(case, out=None, workspace=None, status=None, stream=None, yarn=None):
+    """Run the op on a ``workloads.Case`` whose tensors are on the GPU
+    (``yarn``: YaRN RoPE for the fused variant)."""
     if out is None:
         out = torch.empty(case.T, case.Hq * case.D, dtype=torch.bfloat16, device=case.qkv.device)
     if workspace is None:
@@ -225,7 +259,7 @@ def run_case(case, out=None, workspace=None, status=None, stream=None):
     if case.qknorm:
         return k3da_attn_qknorm(out, case.qkv, case.pool, case.page_table, case.ctx_lens,
                                 case.positions, case.q_norm_w, case.k_norm_w, eps=case.eps,
-                                rope_base=case.rope_base, **kw)
+                                rope_base=case.rope_base, yarn=yarn, **kw)
     return k3da_attn(out, case.qkv, case.pool, case.page_table, case.ctx_lens, **kw)
 
 

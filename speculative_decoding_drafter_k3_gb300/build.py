@@ -13,7 +13,7 @@ import sys
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 SOURCES = [os.path.join(PKG, "csrc", "k3da.cu"), os.path.join(PKG, "csrc", "k3da_norm_rope.cu")]
-HEADERS = [os.path.join(ROOT, "include", "k3da.h")]
+HEADERS = [os.path.join(ROOT, "include", "k3da.h"), os.path.join(PKG, "csrc", "rope_table.h")]
 LIB = os.path.join(PKG, "libk3da.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

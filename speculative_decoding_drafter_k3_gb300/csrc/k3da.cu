@@ -50,6 +50,7 @@
 #include <mutex>
 
 #include "k3da.h"
+#include "rope_table.h"
 
 namespace {
 
@@ -116,6 +117,7 @@ struct Params {
     int grid;           // CTAs of the split pass
     float scale_log2;   // softmax_scale * log2(e)
     float eps;
+    float rope_mscale;  // multiplier of the rotated q and k (YaRN), 1 for plain RoPE
     double inv_freq[kD / 2];
 };
 
@@ -701,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     red = fma(-turns, 2.4492935982947064e-16, red);
                     float sn, cs;
                     sincosf(static_cast<float>(red), &sn, &cs);
-                    trig[e] = make_float2(cs, sn);
+                    trig[e] = make_float2(cs * p.rope_mscale, sn * p.rope_mscale);
                 }
             }
         }
@@ -1380,7 +1382,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                         red = fma(-turns, 2.4492935982947064e-16, red);
                         float sn, cs;
                         sincosf(static_cast<float>(red), &sn, &cs);
-                        trig[e] = make_float2(cs, sn);
+                        trig[e] = make_float2(cs * p.rope_mscale, sn * p.rope_mscale);
                     }
                 }
             }
@@ -1882,7 +1884,8 @@ int static_scratch_address(int dev, void **out) {
 int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, const int32_t *page_table,
            int page_stride, const int32_t *ctx_lens, int R, int B, int Hq, int Hkv, int head_dim,
            float softmax_scale, bool qknorm, const void *positions, int pos_dtype, const void *q_norm_w,
-           const void *k_norm_w, float eps, float rope_base, void *workspace, size_t workspace_bytes,
+           const void *k_norm_w, float eps, float rope_base, const k3da_yarn *yarn, void *workspace,
+           size_t workspace_bytes,
            int32_t *status, void *stream) {
     if (!out || !qkv || !kv_pool || !page_table || !ctx_lens) return K3DA_EINVAL;
     if (!aligned(out, 16) || !aligned(qkv, 16) || !aligned(kv_pool, 16) || !aligned(page_table, 4) ||
@@ -1900,6 +1903,7 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
             !aligned(k_norm_w, 2))
             return K3DA_EINVAL;
         if (!(eps >= 0.f) || !isfinite(eps) || !(rope_base > 1.f) || !isfinite(rope_base)) return K3DA_EINVAL;
+        if (yarn != nullptr && !k3da_host::yarn_valid(yarn)) return K3DA_EINVAL;
     }
     if (!workspace || !aligned(workspace, 16)) return K3DA_EWORKSPACE;
 
@@ -1946,8 +1950,8 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
     prm.grid = cfg.sms * occ;
     prm.scale_log2 = softmax_scale * 1.4426950408889634f;
     prm.eps = eps;
-    for (int j = 0; j < kD / 2; ++j)
-        prm.inv_freq[j] = pow(static_cast<double>(rope_base), -2.0 * j / static_cast<double>(kD));
+    k3da_host::rope_frequencies(prm.inv_freq, kD / 2, rope_base, yarn);
+    prm.rope_mscale = yarn != nullptr ? yarn->mscale : 1.0f;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (qknorm)
@@ -1992,7 +1996,7 @@ int k3da_attn(void *out, const void *qkv, const void *kv_pool, int64_t num_pages
               int32_t *status, void *stream) {
     return launch(out, qkv, kv_pool, num_pages, page_table, page_stride, ctx_lens, num_requests, block_len,
                   num_q_heads, num_kv_heads, head_dim, softmax_scale, false, nullptr, 0, nullptr, nullptr, 0.f,
-                  0.f, workspace, workspace_bytes, status, stream);
+                  0.f, nullptr, workspace, workspace_bytes, status, stream);
 }
 
 int k3da_attn_qknorm(void *out, const void *qkv, const void *kv_pool, int64_t num_pages,
@@ -2002,7 +2006,19 @@ int k3da_attn_qknorm(void *out, const void *qkv, const void *kv_pool, int64_t nu
                      float rope_base, void *workspace, size_t workspace_bytes, int32_t *status, void *stream) {
     return launch(out, qkv, kv_pool, num_pages, page_table, page_stride, ctx_lens, num_requests, block_len,
                   num_q_heads, num_kv_heads, head_dim, softmax_scale, true, positions, pos_dtype, q_norm_w,
-                  k_norm_w, eps, rope_base, workspace, workspace_bytes, status, stream);
+                  k_norm_w, eps, rope_base, nullptr, workspace, workspace_bytes, status, stream);
+}
+
+int k3da_attn_qknorm_yarn(void *out, const void *qkv, const void *kv_pool, int64_t num_pages,
+                          const int32_t *page_table, int page_stride, const int32_t *ctx_lens, int num_requests,
+                          int block_len, int num_q_heads, int num_kv_heads, int head_dim, float softmax_scale,
+                          const void *positions, int pos_dtype, const void *q_norm_w, const void *k_norm_w,
+                          float eps, float rope_base, const k3da_yarn *yarn, void *workspace,
+                          size_t workspace_bytes, int32_t *status, void *stream) {
+    if (!k3da_host::yarn_valid(yarn)) return K3DA_EINVAL;
+    return launch(out, qkv, kv_pool, num_pages, page_table, page_stride, ctx_lens, num_requests, block_len,
+                  num_q_heads, num_kv_heads, head_dim, softmax_scale, true, positions, pos_dtype, q_norm_w,
+                  k_norm_w, eps, rope_base, yarn, workspace, workspace_bytes, status, stream);
 }
 
 int k3da_attn_qknorm_noalloc(void *out, const void *qkv, const void *kv_pool, int64_t num_pages,
@@ -2019,7 +2035,7 @@ int k3da_attn_qknorm_noalloc(void *out, const void *qkv, const void *kv_pool, in
     if (rc != K3DA_OK) return rc;
     return launch(out, qkv, kv_pool, num_pages, page_table, page_stride, ctx_lens, num_requests, block_len,
                   num_q_heads, num_kv_heads, head_dim, softmax_scale, true, positions, pos_dtype, q_norm_w,
-                  k_norm_w, eps, rope_base, scratch, kStaticScratchBytes, status, stream);
+                  k_norm_w, eps, rope_base, nullptr, scratch, kStaticScratchBytes, status, stream);
 }
 
 size_t k3da_noalloc_scratch_bytes(void) { return kStaticScratchBytes; }

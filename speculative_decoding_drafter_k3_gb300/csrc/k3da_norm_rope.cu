@@ -6,7 +6,9 @@
 // NVFP4 support on SM103" (NVIDIA/TensorRT-LLM PR #20532): per token, per
 // head, RMSNorm over the 64 dims (eps 1e-5, one weight vector for q and one
 // for k) followed by NeoX RoPE (pairs (j, j+32), base 10000), in place on the
-// q and k heads of qkv; v heads are left alone.
+// q and k heads of qkv; v heads are left alone.  k3da_qk_norm_rope_yarn
+// turns the pairs by the YaRN frequencies of k3da_yarn instead and scales
+// the rotated values by its mscale.
 //
 // Design: the work is a few KB per token, so the call is launch- and
 // latency-bound.  One warp per (token, q-or-k head) row; lane j holds the
@@ -23,6 +25,7 @@
 #include <cstring>
 
 #include "k3da.h"
+#include "rope_table.h"
 
 namespace {
 
@@ -39,6 +42,7 @@ struct NormRopeParams {
     int Hq, Hkv;
     int pos_i64;
     float eps;
+    float mscale;  // multiplier of the rotated q and k (YaRN), 1 for plain RoPE
     double inv_freq[kD / 2];
 };
 
@@ -67,17 +71,17 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) k3da_norm_rope_kernel(const 
     red = fma(-turns, 2.4492935982947064e-16, red);            // 2 pi, low part
     float sn, cs;
     sincosf(static_cast<float>(red), &sn, &cs);
+    cs *= p.mscale;
+    sn *= p.mscale;
     x[lane] = __float2bfloat16_rn(n_lo * cs - n_hi * sn);
     x[lane + 32] = __float2bfloat16_rn(n_hi * cs + n_lo * sn);
 }
 
 bool aligned_to(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-}  // namespace
-
-extern "C" int k3da_qk_norm_rope(void *qkv, int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
-                                 const void *positions, int pos_dtype, const void *q_norm_w,
-                                 const void *k_norm_w, float eps, float rope_base, void *stream) {
+int launch_norm_rope(void *qkv, int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                     const void *positions, int pos_dtype, const void *q_norm_w, const void *k_norm_w, float eps,
+                     float rope_base, const k3da_yarn *yarn, void *stream) {
     if (!qkv || !positions || !q_norm_w || !k_norm_w) return K3DA_EINVAL;
     if (num_tokens < 1) return K3DA_EINVAL;
     if (head_dim != kD) return K3DA_EUNSUPPORTED;
@@ -100,11 +104,29 @@ extern "C" int k3da_qk_norm_rope(void *qkv, int num_tokens, int num_q_heads, int
     prm.Hkv = num_kv_heads;
     prm.pos_i64 = pos_dtype == K3DA_POS_I64;
     prm.eps = eps;
-    for (int j = 0; j < kD / 2; ++j)
-        prm.inv_freq[j] = std::pow(static_cast<double>(rope_base), -2.0 * j / static_cast<double>(kD));
+    k3da_host::rope_frequencies(prm.inv_freq, kD / 2, rope_base, yarn);
+    prm.mscale = yarn != nullptr ? yarn->mscale : 1.0f;
     const long long ctas = (prm.rows + kRowsPerCta - 1) / kRowsPerCta;
     if (ctas > 0x7fffffffLL) return K3DA_EINVAL;
     k3da_norm_rope_kernel<<<static_cast<unsigned>(ctas), 32 * kRowsPerCta, 0, static_cast<cudaStream_t>(stream)>>>(
         prm);
     return cudaGetLastError() == cudaSuccess ? K3DA_OK : K3DA_ECUDA;
+}
+
+}  // namespace
+
+extern "C" int k3da_qk_norm_rope(void *qkv, int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                                 const void *positions, int pos_dtype, const void *q_norm_w,
+                                 const void *k_norm_w, float eps, float rope_base, void *stream) {
+    return launch_norm_rope(qkv, num_tokens, num_q_heads, num_kv_heads, head_dim, positions, pos_dtype, q_norm_w,
+                            k_norm_w, eps, rope_base, nullptr, stream);
+}
+
+extern "C" int k3da_qk_norm_rope_yarn(void *qkv, int num_tokens, int num_q_heads, int num_kv_heads,
+                                      int head_dim, const void *positions, int pos_dtype, const void *q_norm_w,
+                                      const void *k_norm_w, float eps, float rope_base, const k3da_yarn *yarn,
+                                      void *stream) {
+    if (!k3da_host::yarn_valid(yarn)) return K3DA_EINVAL;
+    return launch_norm_rope(qkv, num_tokens, num_q_heads, num_kv_heads, head_dim, positions, pos_dtype, q_norm_w,
+                            k_norm_w, eps, rope_base, yarn, stream);
 }

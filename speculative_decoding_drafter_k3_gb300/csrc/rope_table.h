@@ -1,0 +1,41 @@
+// rope_table.h -- host side of the rotary frequencies shared by the library's
+// kernels: the plain NeoX table and its YaRN rescaling (k3da_yarn in k3da.h).
+#pragma once
+
+#include <cmath>
+
+#include "k3da.h"
+
+namespace k3da_host {
+
+// True when `y` describes a usable YaRN rescaling.
+inline bool yarn_valid(const k3da_yarn *y) {
+    if (y == nullptr) return false;
+    const float v[5] = {y->factor, y->original_max_position, y->beta_fast, y->beta_slow, y->mscale};
+    for (float x : v)
+        if (!std::isfinite(x)) return false;
+    return y->factor >= 1.f && y->original_max_position > 0.f && y->beta_slow > 0.f &&
+           y->beta_fast > y->beta_slow && y->mscale > 0.f;
+}
+
+// Frequencies of the `pairs` rotary pairs of a head of 2*pairs dims, in
+// fp64.  Plain NeoX: theta_j = base^(-2j / dims).  With YaRN (factor != 1):
+// r = original_max_position * theta_j / (2 pi) counts the pair's turns over
+// the original context; pairs with r >= beta_fast keep theta_j, pairs with
+// r <= beta_slow turn factor times slower, and a linear ramp joins the two.
+inline void rope_frequencies(double *inv_freq, int pairs, float base, const k3da_yarn *yarn) {
+    const double dims = 2.0 * pairs;
+    for (int j = 0; j < pairs; ++j) {
+        const double theta = std::pow(static_cast<double>(base), -2.0 * j / dims);
+        if (yarn == nullptr || yarn->factor == 1.f) {
+            inv_freq[j] = theta;
+            continue;
+        }
+        const double turns = static_cast<double>(yarn->original_max_position) * theta / 6.283185307179586;
+        double ramp = (turns - yarn->beta_slow) / (static_cast<double>(yarn->beta_fast) - yarn->beta_slow);
+        ramp = ramp < 0.0 ? 0.0 : (ramp > 1.0 ? 1.0 : ramp);
+        inv_freq[j] = theta * ramp + theta / static_cast<double>(yarn->factor) * (1.0 - ramp);
+    }
+}
+
+}  // namespace k3da_host

@@ -164,3 +164,29 @@ def call_norm_rope(lib, **over):
 ])
 def test_norm_rope_refuses_out_of_contract_calls(lib, over, code):
     assert call_norm_rope(lib, **over) == code
+
+
+def _yarn(**over):
+    y = dict(factor=4.0, original_max_position=4096.0, beta_fast=32.0, beta_slow=1.0, mscale=1.1386)
+    y.update(over)
+    return k3da.Yarn(**y)
+
+
+@pytest.mark.parametrize("over", [dict(factor=0.5), dict(factor=float("nan")), dict(original_max_position=0.0),
+                                  dict(beta_fast=1.0), dict(beta_slow=0.0), dict(mscale=0.0),
+                                  dict(mscale=float("inf"))])
+def test_yarn_calls_refuse_bad_scaling(lib, over):
+    y = _yarn(**over)
+    assert lib.k3da_qk_norm_rope_yarn(FAKE, 64, 6, 1, 64, FAKE, k3da.POS_I64, FAKE, FAKE, 1e-5, 10000.0,
+                                      ctypes.byref(y), None) == k3da.EINVAL
+    assert lib.k3da_attn_qknorm_yarn(FAKE, FAKE, FAKE, 16, FAKE, 4, FAKE, 8, 8, 6, 1, 64, 0.125, FAKE,
+                                     k3da.POS_I64, FAKE, FAKE, 1e-5, 10000.0, ctypes.byref(y), FAKE, 1 << 30,
+                                     None, None) == k3da.EINVAL
+
+
+def test_yarn_calls_refuse_a_missing_spec(lib):
+    assert lib.k3da_qk_norm_rope_yarn(FAKE, 64, 6, 1, 64, FAKE, k3da.POS_I64, FAKE, FAKE, 1e-5, 10000.0,
+                                      None, None) == k3da.EINVAL
+    assert lib.k3da_attn_qknorm_yarn(FAKE, FAKE, FAKE, 16, FAKE, 4, FAKE, 8, 8, 6, 1, 64, 0.125, FAKE,
+                                     k3da.POS_I64, FAKE, FAKE, 1e-5, 10000.0, None, FAKE, 1 << 30,
+                                     None, None) == k3da.EINVAL

@@ -61,6 +61,8 @@ def parse():
                     help="attn: the block attention (headline); qk_norm_rope: the standalone "
                          "fused q/k norm + RoPE call on --tokens tokens of --heads heads")
     ap.add_argument("--tokens", type=int, default=64)
+    ap.add_argument("--yarn", action="store_true",
+                    help="YaRN RoPE (factor 4, original context 4096, beta 32/1, mscale 0.1 ln 4 + 1)")
     ap.add_argument("--heads", choices=["6/1", "24/4"], default="24/4")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -308,8 +310,10 @@ def run_ours(args, world, rank):
 
     flush = _Flush()
 
+    yarn = k3da.Yarn.of(4.0, 4096.0) if args.yarn and case.qknorm else None
+
     def call():
-        k3da.run_case(case, out=out, workspace=ws, status=status)
+        k3da.run_case(case, out=out, workspace=ws, status=status, yarn=yarn)
 
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
@@ -378,7 +382,7 @@ def run_ours(args, world, rank):
 
         def step_e2e():
             dev_pack.copy_(host_pack, non_blocking=True)
-            k3da.run_case(case_e2e, out=out, workspace=ws, status=status)
+            k3da.run_case(case_e2e, out=out, workspace=ws, status=status, yarn=yarn)
             host_out.copy_(out, non_blocking=True)
 
         for _ in range(3):
@@ -418,6 +422,7 @@ def run_ours(args, world, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",
             "data": "synthetic (seeded N(0,1) bf16 pool/qkv, random page permutation)",
             "config": config_of(case, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                                       "rope": "yarn(4.0, 4096, 32, 1)" if yarn is not None else "neox",
                                        "split_ctas": k3da.split_grid(dev.index)}),
             "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clock_info,
             "median_call_us": statistics.median(call_ms) * 1e3,
@@ -447,8 +452,10 @@ def run_norm_rope(args, world, rank):
     pos = torch.randint(0, 1 << 17, (T,), generator=g, dtype=torch.int64).to(dev)
     flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
+    yarn = k3da.Yarn.of(4.0, 4096.0) if args.yarn else None
+
     def call():
-        k3da.k3da_qk_norm_rope(qkv, pos, qw, kw, num_q_heads=Hq, num_kv_heads=Hkv)
+        k3da.k3da_qk_norm_rope(qkv, pos, qw, kw, num_q_heads=Hq, num_kv_heads=Hkv, yarn=yarn)
 
     for _ in range(max(args.warmup, 3)):
         call()

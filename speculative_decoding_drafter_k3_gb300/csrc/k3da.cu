@@ -79,7 +79,7 @@ constexpr int kChunkTarget = 304;  // ... or, with few units, about this many ch
 #define K3DA_CHUNK_MAX 32
 #endif
 constexpr int kChunkMax = K3DA_CHUNK_MAX;  // ... of at most this many pages, beyond which it gets more chunks
-constexpr int kPartialFloats = kRows * kD;    // O of one (CTA, unit) range
+constexpr int kPartialElems = kRows * kD;     // O of one chunk, bf16
 constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -107,7 +107,7 @@ struct Params {
     const __nv_bfloat16 *q_w;
     const __nv_bfloat16 *k_w;
     int *ws_units;      // [2][32]: first chunk slot and chunk count of each unit
-    float *ws_o;        // [slots][48][64]
+    __nv_bfloat16 *ws_o;  // [slots][48][64]: a chunk's unnormalised O, rounded to bf16 once
     float2 *ws_ml;      // [slots][48]  (m in log2 units, l)
     int32_t *status;
     long long num_pages;
@@ -809,15 +809,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 const long long slot = static_cast<long long>(pl->cstart[u]) + jc;
                 const int ra = rb * 16 + (lane >> 2), rbw = ra + 8;
-                float *ob = p.ws_o + slot * kPartialFloats;
+                __nv_bfloat16 *ob = p.ws_o + slot * kPartialElems;
                 const int dq = 2 * (lane & 3);
 #pragma unroll
                 for (int nd = 0; nd < 8; ++nd) {
                     if (ra < rows)
-                        *reinterpret_cast<float2 *>(ob + ra * kD + nd * 8 + dq) = make_float2(st.o[nd][0], st.o[nd][1]);
+                        *reinterpret_cast<uint32_t *>(ob + ra * kD + nd * 8 + dq) = pack_bf16(st.o[nd][0], st.o[nd][1]);
                     if (rbw < rows)
-                        *reinterpret_cast<float2 *>(ob + rbw * kD + nd * 8 + dq) =
-                            make_float2(st.o[nd][2], st.o[nd][3]);
+                        *reinterpret_cast<uint32_t *>(ob + rbw * kD + nd * 8 + dq) = pack_bf16(st.o[nd][2], st.o[nd][3]);
                 }
                 if ((lane & 3) == 0) {
                     if (ra < rows) p.ws_ml[slot * kRows + ra] = make_float2(st.m[0], st.l[0]);
@@ -1326,11 +1325,16 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                 outv[j] = keep + __shfl_xor_sync(kFull, give, 16);
             }
             if (active) {
-                float4 *dst = reinterpret_cast<float4 *>(p.ws_o + epi_slot * kPartialFloats + rho * kD +
-                                                         kDimsPerSet * set + kKeep * half);
+                // The partial's O leaves as bf16: half the bytes for the
+                // split pass to write and the combine to read; one rounding
+                // (2^-9 relative) of values the combine then averages.
+                uint4 *dst = reinterpret_cast<uint4 *>(p.ws_o + epi_slot * kPartialElems + rho * kD +
+                                                       kDimsPerSet * set + kKeep * half);
 #pragma unroll
-                for (int j = 0; j < kKeep / 4; ++j)
-                    dst[j] = make_float4(outv[4 * j], outv[4 * j + 1], outv[4 * j + 2], outv[4 * j + 3]);
+                for (int j = 0; j < kKeep / 8; ++j)
+                    dst[j] = make_uint4(pack_bf16(outv[8 * j], outv[8 * j + 1]), pack_bf16(outv[8 * j + 2], outv[8 * j + 3]),
+                                        pack_bf16(outv[8 * j + 4], outv[8 * j + 5]),
+                                        pack_bf16(outv[8 * j + 6], outv[8 * j + 7]));
                 if (half == 0 && set == 0) p.ws_ml[epi_slot * kRows + rho] = make_float2(epi_m, ltot);
             }
             epi_pending = false;
@@ -1668,10 +1672,11 @@ __global__ void __launch_bounds__(128) k3da_combine_kernel(const __grid_constant
                 if (j < nch) {
                     const long long slot = slot0 + j;
                     ml[f] = p.ws_ml[slot * kRows + row];
-                    const float4 *src =
-                        reinterpret_cast<const float4 *>(p.ws_o + slot * kPartialFloats + row * kD + dc * 8);
-                    v0[f] = src[0];
-                    v1[f] = src[1];
+                    const uint4 w = *reinterpret_cast<const uint4 *>(p.ws_o + slot * kPartialElems + row * kD + dc * 8);
+                    v0[f] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                                        __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+                    v1[f] = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
+                                        __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
                 } else {
                     ml[f] = make_float2(-INFINITY, 0.f);
                     v0[f] = v1[f] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1850,7 +1855,8 @@ size_t workspace_slots(int R, int Hkv, int page_stride) {
 constexpr size_t kWsHeaderBytes = 512;  // unit table, then the partials (16-byte aligned)
 
 size_t workspace_for(int R, int Hkv, int page_stride) {
-    return kWsHeaderBytes + workspace_slots(R, Hkv, page_stride) * (kPartialFloats * sizeof(float) + kRows * sizeof(float2));
+    return kWsHeaderBytes +
+           workspace_slots(R, Hkv, page_stride) * (kPartialElems * sizeof(__nv_bfloat16) + kRows * sizeof(float2));
 }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -1936,8 +1942,8 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
     prm.k_w = static_cast<const __nv_bfloat16 *>(k_norm_w);
     const size_t slots = workspace_slots(R, Hkv, page_stride);
     prm.ws_units = static_cast<int *>(workspace);
-    prm.ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + kWsHeaderBytes);
-    prm.ws_ml = reinterpret_cast<float2 *>(prm.ws_o + slots * kPartialFloats);
+    prm.ws_o = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(workspace) + kWsHeaderBytes);
+    prm.ws_ml = reinterpret_cast<float2 *>(prm.ws_o + slots * kPartialElems);
     prm.status = status;
     prm.num_pages = num_pages;
     prm.page_stride = page_stride;

@@ -118,7 +118,7 @@ def test_workspace_size_depends_on_shapes_only(lib):
     assert ws(8, 8, 24, 4, 2048) > ws(1, 8, 24, 4, 2048)
     # With long rows every unit has ceil((stride+1)/32) slots of the same size.
     slot = (ws(8, 8, 24, 4, 4096 - 1) - ws(8, 8, 24, 4, 2048 - 1)) // (32 * (128 - 64))
-    assert slot == 48 * 64 * 4 + 48 * 8
+    assert slot == 48 * 64 * 2 + 48 * 8  # bf16 O and fp32 (m, l) per row
     assert ws(8, 8, 24, 4, 2048 - 1) - ws(4, 8, 24, 4, 2048 - 1) == 16 * 64 * slot
 
 

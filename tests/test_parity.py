@@ -64,6 +64,20 @@ def test_edge_lengths(lens, Hq, Hkv):
     check(case)
 
 
+@pytest.mark.parametrize("R,B", [(1, 1), (1, 8), (3, 5), (5, 3), (8, 1)])
+@pytest.mark.parametrize("qknorm,pos_dtype", [(True, torch.int32), (True, torch.int64), (False, torch.int32)])
+def test_heads_24_4_request_token_splits(R, B, qknorm, pos_dtype):
+    """The 24/4 layout over request x token splits, both position types and
+    the plain variant; lengths from the split sweep's set plus a 10k context."""
+    g = torch.Generator().manual_seed(700 + 10 * R + B)
+    choices = workloads.SWEEP_LENGTHS + [10000]
+    lens = [choices[int(i)] for i in torch.randint(0, len(choices), (R,), generator=g)]
+    case = workloads.build_case(f"h24_{R}x{B}", R=R, B=B, Hq=24, Hkv=4, lens=lens, page_stride=160,
+                                num_pages=R * 160, qknorm=qknorm, pos_dtype=pos_dtype, seed=71 + R * B,
+                                device="cuda")
+    check(case)
+
+
 def test_single_token_single_request():
     case = workloads.build_case("1x1", R=1, B=1, Hq=24, Hkv=4, lens=[777], page_stride=13,
                                 num_pages=40, qknorm=True, seed=61, device="cuda")

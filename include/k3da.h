@@ -255,6 +255,18 @@ int k3da_qk_norm_rope_yarn(void *qkv, int num_tokens, int num_q_heads, int num_k
 /* Static description of a k3da_error or K3DA_STATUS_* bit set. */
 const char *k3da_error_string(int code);
 
+/*
+ * k3da_selftest_wait_timeout -- diagnostic of the failure path: launches one
+ * CTA that waits, through the same bounded wait every kernel here uses, on a
+ * barrier nothing completes.  Warp 0 gives up after limit_ns (1 ns .. 2 s)
+ * and raises the abort flag; the other warps must leave on the flag.  The
+ * kernel ORs K3DA_STATUS_TIMEOUT into *status (a device int32 the caller
+ * clears), and 0x100 if a wait that can never complete did.  The context
+ * stays usable.  K3DA_EINVAL on a NULL/misaligned status or a limit out of
+ * range.
+ */
+int k3da_selftest_wait_timeout(int32_t *status, unsigned long long limit_ns, void *stream);
+
 /* Library version, major*10000 + minor*100 + patch. */
 int k3da_version(void);
 

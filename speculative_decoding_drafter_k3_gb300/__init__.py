@@ -38,7 +38,7 @@ POS_I32, POS_I64 = 0, 1
 EXPORTED = ["k3da_workspace_bytes", "k3da_attn", "k3da_attn_qknorm", "k3da_attn_qknorm_noalloc",
             "k3da_noalloc_scratch_bytes", "k3da_split_grid", "k3da_set_phase_event",
             "k3da_error_string", "k3da_version", "k3da_qk_norm_rope", "k3da_attn_qknorm_yarn",
-            "k3da_qk_norm_rope_yarn"]
+            "k3da_qk_norm_rope_yarn", "k3da_selftest_wait_timeout"]
 
 
 class Yarn(ctypes.Structure):
@@ -106,6 +106,8 @@ def load_library():
         lib.k3da_attn_qknorm_yarn.restype = c_int
         lib.k3da_qk_norm_rope_yarn.argtypes = [vp, c_int, c_int, c_int, c_int, vp, c_int, vp, vp, c_f, c_f, yp, vp]
         lib.k3da_qk_norm_rope_yarn.restype = c_int
+        lib.k3da_selftest_wait_timeout.argtypes = [vp, ctypes.c_ulonglong, vp]
+        lib.k3da_selftest_wait_timeout.restype = c_int
         _lib = lib
         return lib
 

@@ -163,12 +163,12 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // TIMEOUT status bit; the caller then carries on without the data so every
 // warp still reaches every named barrier and the CTA exits.
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                            int32_t *status) {
+                                            int32_t *status, unsigned long long limit_ns = kWaitLimitNs) {
     const unsigned long long t0 = global_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             *abort_flag = 1;
             if (status) atomicOr(status, K3DA_STATUS_TIMEOUT);
             return false;
@@ -1731,6 +1731,30 @@ __global__ void __launch_bounds__(128) k3da_combine_kernel(const __grid_constant
     }
 }
 
+// ------------------------------------------------------- wait self-test --
+//
+// Exercises the bounded wait every kernel of the library uses, on an
+// mbarrier that nothing ever completes: warp 0 waits with a short limit and
+// must give up, raise the CTA's abort flag and the TIMEOUT status bit; the
+// other warps wait on the same barrier with the normal 2 s limit and must
+// leave as soon as they see the flag.  A wait that completed would set bit
+// 0x100.  No GPU fault is involved: this is how a stuck wait ends.
+__global__ void __launch_bounds__(128) k3da_wait_selftest_kernel(int32_t *status, unsigned long long limit_ns) {
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ int abort_flag;
+    volatile int *flag = &abort_flag;
+    if (threadIdx.x == 0) {
+        *flag = 0;
+        mbar_init(smem_u32(&bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const bool done = threadIdx.x < 32 ? mbar_wait_slow(smem_u32(&bar), 0, flag, status, limit_ns)
+                                       : mbar_wait_slow(smem_u32(&bar), 0, flag, status);
+    if (done) atomicOr(status, 0x100);
+    __syncthreads();
+}
+
 // The split pass that runs: the tcgen05 one unless built with
 // K3DA_USE_TCGEN05=0 (the mma.sync one).
 #ifndef K3DA_USE_TCGEN05
@@ -2074,5 +2098,11 @@ const char *k3da_error_string(int code) {
 }
 
 int k3da_version(void) { return 100; }
+
+int k3da_selftest_wait_timeout(int32_t *status, unsigned long long limit_ns, void *stream) {
+    if (!status || !aligned(status, 4) || limit_ns == 0 || limit_ns > kWaitLimitNs) return K3DA_EINVAL;
+    k3da_wait_selftest_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_ns);
+    return cudaGetLastError() == cudaSuccess ? K3DA_OK : K3DA_ECUDA;
+}
 
 }  // extern "C"

@@ -190,3 +190,10 @@ def test_yarn_calls_refuse_a_missing_spec(lib):
     assert lib.k3da_attn_qknorm_yarn(FAKE, FAKE, FAKE, 16, FAKE, 4, FAKE, 8, 8, 6, 1, 64, 0.125, FAKE,
                                      k3da.POS_I64, FAKE, FAKE, 1e-5, 10000.0, None, FAKE, 1 << 30,
                                      None, None) == k3da.EINVAL
+
+
+def test_wait_selftest_refuses_bad_arguments(lib):
+    assert lib.k3da_selftest_wait_timeout(None, 1000000, None) == k3da.EINVAL
+    assert lib.k3da_selftest_wait_timeout(FAKE + 2, 1000000, None) == k3da.EINVAL
+    assert lib.k3da_selftest_wait_timeout(FAKE, 0, None) == k3da.EINVAL
+    assert lib.k3da_selftest_wait_timeout(FAKE, 3_000_000_000, None) == k3da.EINVAL

@@ -137,3 +137,27 @@ def test_graph_replay_with_rewritten_inputs(maker):
         torch.cuda.synchronize()
         assert torch.equal(replayed.view(torch.int16), eager.view(torch.int16))
         assert_close(replayed, oracle_for(case), f"replay seed {seed}")
+
+
+def test_a_stuck_wait_times_out_with_a_status_and_the_context_survives():
+    """Failure detection without a fault: a wait on a barrier nothing
+    completes gives up after its limit, raises TIMEOUT, releases the other
+    warps, and later calls run normally."""
+    import time
+    lib = k3da.load_library()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    rc = lib.k3da_selftest_wait_timeout(ctypes_ptr(status), 5_000_000, None)  # 5 ms
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert rc == k3da.OK
+    assert int(status.item()) == k3da.STATUS_TIMEOUT
+    assert elapsed < 1.0, f"the other warps did not leave on the abort flag ({elapsed:.2f} s)"
+    case = workloads.mixed_8x8(device="cuda")
+    assert_close(k3da.run_case(case), oracle_for(case), "after a timed-out wait")
+
+
+def ctypes_ptr(t):
+    import ctypes
+    return ctypes.c_void_p(t.data_ptr())

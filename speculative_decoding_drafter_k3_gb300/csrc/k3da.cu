@@ -22,22 +22,24 @@
 //     and every chunk's partial result is the same whatever the other
 //     requests hold: requests are isolated bit for bit.  The plan is built on
 //     the device from ctx_lens, so a captured graph replays with new lengths.
-//   * A CTA = 6 consumer warps + 1 producer warp.  Consumer warp w owns query
-//     rows 16*(w%3)..+15 (the 6 q heads x B tokens = 48 rows that share one
-//     kv head) and keys 32*(w/3)..+31 of every page.  The producer walks the
-//     page table (32 ids per coalesced load, prefetched a batch ahead) and
-//     TMA-loads each page's K tile and V tile (64 x 64 bf16, 8 KB each,
-//     contiguous in the HND pool) into a ring of shared-memory stages with
-//     the 128-byte swizzle, so the ldmatrix reads below are conflict-free.
-//   * Consumers: S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 in,
-//     fp32 accumulate), online softmax in base 2 with the scale folded in.
-//     When a CTA starts on a unit, its q (and block k, v) rows are staged
+//   * The split pass (k3da_tc_kernel, below) runs on the 5th-generation
+//     tensor cores: a producer warp walks the page table (32 ids per
+//     coalesced load, a batch ahead) and TMA-loads each page's K and V tiles
+//     (64 x 64 bf16, 8 KB each, contiguous in the HND pool, 128-byte
+//     swizzle) into a ring of shared-memory stages; one warp issues
+//     S = Q K^T and another O += P V as tcgen05.mma with TMEM accumulators;
+//     four row warps run the online softmax (base 2, scale folded in, lazy
+//     rescale) and hand P to the P.V product through TMEM.
+//   * When a CTA starts on a unit, its q (and block k, v) rows are staged
 //     with one batch of cp.async copies and turned into operand tiles:
 //     RMSNorm and RoPE happen on the way in, RoPE angles are reduced in fp64
 //     then turned by an accurate sincosf.
-//   * Each chunk leaves an unnormalised partial (O, m, l) in the workspace;
-//     the combine kernel folds a unit's chunk partials in a fixed order and
-//     writes bf16 out, so reruns are bit-identical.
+//   * k3da_split_kernel, the first design (6 consumer warps with mma.sync
+//     m16n8k16 and ldmatrix, + 1 producer warp), is kept as the
+//     legacy-tensor-core baseline: built with -DK3DA_USE_TCGEN05=0.
+//   * Each chunk leaves an unnormalised partial (O as bf16, m and l in fp32)
+//     in the workspace; the combine kernel folds a unit's chunk partials in
+//     a fixed order and writes bf16 out, so reruns are bit-identical.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>

@@ -197,3 +197,24 @@ def test_wait_selftest_refuses_bad_arguments(lib):
     assert lib.k3da_selftest_wait_timeout(FAKE + 2, 1000000, None) == k3da.EINVAL
     assert lib.k3da_selftest_wait_timeout(FAKE, 0, None) == k3da.EINVAL
     assert lib.k3da_selftest_wait_timeout(FAKE, 3_000_000_000, None) == k3da.EINVAL
+
+
+def test_binding_refuses_host_tensors_before_any_call(lib):
+    import torch
+    from speculative_decoding_drafter_k3_gb300 import workloads
+    case = workloads.tiny()  # CPU tensors: the binding must refuse them, never fall back
+    out = torch.empty(case.T, case.Hq * 64, dtype=torch.bfloat16)
+    ws = torch.empty(1 << 20, dtype=torch.uint8)
+    with pytest.raises(k3da.K3daError):
+        k3da.k3da_attn(out, case.qkv, case.pool, case.page_table, case.ctx_lens, block_len=case.B,
+                       num_q_heads=case.Hq, num_kv_heads=case.Hkv, workspace=ws)
+    with pytest.raises(k3da.K3daError):
+        k3da.k3da_qk_norm_rope(case.qkv, torch.zeros(case.T, dtype=torch.int64), torch.ones(64, dtype=torch.bfloat16),
+                               torch.ones(64, dtype=torch.bfloat16), num_q_heads=6, num_kv_heads=1)
+
+
+def test_workspace_query_through_the_binding(lib):
+    n = k3da.workspace_bytes(8, 8, 24, 4, 2048)
+    assert n == lib.k3da_workspace_bytes(8, 8, 24, 4, 2048) > 512
+    with pytest.raises(k3da.K3daError):
+        k3da.workspace_bytes(9, 8, 24, 4, 2048)

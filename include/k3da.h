@@ -155,7 +155,7 @@ int k3da_set_phase_event(void *event);
  * and output.
  *
  * - Sizes whose workspace (k3da_workspace_bytes) exceeds the array are
- *   refused with K3DA_EWORKSPACE: page_stride <= 511 always fits.
+ *   refused with K3DA_EWORKSPACE: page_stride <= 1279 always fits.
  * - Nothing is allocated or freed, by the library or by any routine it
  *   calls.
  * - The first call on a device looks up the array's device address (with

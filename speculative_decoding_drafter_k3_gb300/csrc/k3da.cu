@@ -86,7 +86,7 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
-constexpr int kOffStages = 0;
+[[maybe_unused]] constexpr int kOffStages = 0;
 constexpr int kOffQ = kStages * kStageBytes;          // 48 rows x 128 B
 constexpr int kOffBlkK = kOffQ + kRows * 128;         // 16 rows x 128 B
 constexpr int kOffBlkV = kOffBlkK + 16 * 128;
@@ -97,7 +97,7 @@ constexpr int kOffPlan = kOffMerge + kRowWarps * 36 * 32 * 4;  // struct Plan
 constexpr int kOffBar = kOffPlan + 1536;              // 2*kStages mbarriers
 constexpr int kOffFlag = kOffBar + 2 * kStages * 8;
 constexpr int kSmemUsed = kOffFlag + 16;
-constexpr int kSmemBytes = kSmemUsed + 1024;          // slack for alignment
+[[maybe_unused]] constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for alignment
 static_assert(kOffBar % 8 == 0 && kOffPlan % 8 == 0, "mbarrier / int64 alignment");
 
 struct Params {
@@ -197,21 +197,21 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+[[maybe_unused]] __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                         uint32_t &r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr));
 }
 
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+[[maybe_unused]] __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                           uint32_t &r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr));
 }
 
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+[[maybe_unused]] __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
@@ -511,7 +511,7 @@ __device__ __forceinline__ void prep_row(uint8_t *tile, int row, float x_lo, flo
     }
 }
 
-__device__ __forceinline__ void zero_row(uint8_t *tile, int row, int lane) {
+[[maybe_unused]] __device__ __forceinline__ void zero_row(uint8_t *tile, int row, int lane) {
     const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
     *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, lane >> 3) + (lane & 7) * 2) = z;
     *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, 4 + (lane >> 3)) + (lane & 7) * 2) = z;
@@ -525,7 +525,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-__device__ __forceinline__ float bf16_at(const uint8_t *base, int index) {
+[[maybe_unused]] __device__ __forceinline__ float bf16_at(const uint8_t *base, int index) {
     return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[index]);
 }
 
@@ -1011,7 +1011,6 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     constexpr auto kSets = tc::kSets;
     constexpr auto kDimsPerSet = tc::kDimsPerSet;
     constexpr auto kOffPlan = tc::kOffPlan;
-    constexpr auto kNumBars = tc::kNumBars;
     constexpr auto kOffBar = tc::kOffBar;
     constexpr auto kOffTaddr = tc::kOffTaddr;
     constexpr auto kOffFlag = tc::kOffFlag;
@@ -1889,7 +1888,7 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 // Scratch of k3da_attn_qknorm_noalloc: a fixed array in device memory that
 // exists on every GPU this library is loaded on, for callers that cannot
-// allocate.  8 MiB covers every shape with page_stride <= 511.
+// allocate.  8 MiB covers every shape with page_stride <= 1279.
 constexpr size_t kStaticScratchBytes = size_t(8) << 20;
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 

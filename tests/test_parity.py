@@ -78,6 +78,17 @@ def test_heads_24_4_request_token_splits(R, B, qknorm, pos_dtype):
     check(case)
 
 
+def test_lengths_at_full_size_chunk_edges():
+    """8 requests x 24/4 heads (32 units: chunks of 32 pages once a unit has
+    more than ~500 items): contexts whose page counts sit on and next to a
+    chunk edge, a partial last page, one page, and no context."""
+    lens = [639 * 64, 640 * 64, 640 * 64 + 1, 513 * 64 - 5, 512 * 64, 511 * 64 + 63, 64, 0]
+    case = workloads.build_case("chunk_edges", R=8, B=8, Hq=24, Hkv=4, lens=lens, page_stride=641,
+                                num_pages=8 * 641, qknorm=True, pos_dtype=torch.int64, seed=64,
+                                device="cuda")
+    check(case)
+
+
 def test_single_token_single_request():
     case = workloads.build_case("1x1", R=1, B=1, Hq=24, Hkv=4, lens=[777], page_stride=13,
                                 num_pages=40, qknorm=True, seed=61, device="cuda")

@@ -146,8 +146,9 @@ int k3da_set_phase_event(void *event);
  * allocate device memory: code that runs where cudaMalloc is unavailable or
  * forbidden (a host callback, a real-time path that must not allocate, a
  * plugin whose host framework owns every device allocation) or that has no
- * way to keep a workspace buffer between calls.  Not an operation of the ops this library implements
- * (the paper has no counterpart): the same computation as k3da_attn_qknorm,
+ * way to keep a workspace buffer between calls.  An addition of this
+ * library with no counterpart in the drafter's own operations: the same
+ * computation as k3da_attn_qknorm,
  * with the scratch taken from a fixed array of k3da_noalloc_scratch_bytes()
  * (8 MiB) that the library keeps in the memory of every GPU it is loaded on,
  * for the life of the process.  Arguments are those of k3da_attn_qknorm
@@ -191,7 +192,7 @@ int k3da_split_grid(int device);
  * with r_j = original_max_position * theta_j / (2 pi) (its wavelengths in the
  * original context) and the ramp g = clamp((r_j - beta_slow) / (beta_fast -
  * beta_slow), 0, 1), it turns at g * theta_j + (1 - g) * theta_j / factor.
- * Both rotated outputs are multiplied by mscale (the paper's sqrt(1/t), i.e.
+ * Both rotated outputs are multiplied by mscale (the YaRN paper's sqrt(1/t), i.e.
  * 0.1 * ln(factor) + 1, applied to q and k; pass 1 when the model folds it
  * elsewhere).  factor 1 with mscale 1 is plain NeoX RoPE.  Host memory; read
  * during the call only.
@@ -199,8 +200,8 @@ int k3da_split_grid(int device);
 typedef struct {
     float factor;                /* >= 1 */
     float original_max_position; /* > 0 */
-    float beta_fast;             /* > beta_slow (32 in the paper) */
-    float beta_slow;             /* > 0 (1 in the paper) */
+    float beta_fast;             /* > beta_slow (32 in the YaRN paper) */
+    float beta_slow;             /* > 0 (1 in the YaRN paper) */
     float mscale;                /* > 0 */
 } k3da_yarn;
 

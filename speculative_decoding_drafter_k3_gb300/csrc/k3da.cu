@@ -838,11 +838,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 // cores.  An item is the block or a group of kGroup pages (1 by default; 2
 // gives one N = 128 QK^T per two pages but only one CTA per SM).  Row warps
 // w own TMEM lane quarter q = w % 4 (and page w / 4 of a group): query row
-// rho = 12*q + l (l < 12) is copied into Q-tile rows (and TMEM lanes)
-// 32*q + l and 32*q + 16 + l; the thread of the first lane handles keys
-// 0..31 of its page and the thread of the second keys 32..63, so a row's
-// softmax costs two threads half a page each and one shuffle to share the
-// row maximum.  The producer warp streams K/V pages with TMA; one warp issues
+// rho = 12*q + l (l < 12) is Q-tile row (and TMEM lane) 32*q + l.  Threads
+// l and l + 16 of the warp share that lane through the half-split TMEM
+// access (shape 16x32bx2): the first handles keys 0..31 of its page, the
+// second keys 32..63, so a row's softmax costs two threads half a page each
+// and one shuffle to share the row maximum.  The producer warp streams K/V
+// pages with TMA; one warp issues
 // the QK^T products and another the P.V products (a thread issues one MMA
 // at a time, ~156 cycles each at these shapes whatever N, so two issuers
 // double the tensor throughput of a CTA):
@@ -850,11 +851,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 //   O    (128 x 64 fp32, TMEM)  += P[b] (bf16, TMEM) . V_page   (per page)
 // with two S buffers so the next item's QK^T overlaps this item's softmax.
 // The softmax keeps a per-row exponent base m; P = 2^(s*scale*log2e - m) is
-// written as bf16 to TMEM buffer P[b] (each lane's other half of the keys as
-// zeros; kept apart from S[b] so that the next QK^T into S[b] never
+// written as bf16 to TMEM buffer P[b] (each thread its half of the row's
+// keys; kept apart from S[b] so that the next QK^T into S[b] never
 // overwrites a P the previous PV may still be reading) and becomes the A
-// operand of the PV MMA, so each of a row's two lanes accumulates its half
-// of P.V; the halves are added when the chunk's partial is written.  O is
+// operand of the PV MMA, which leaves the row's whole O in its lane.  O is
 // only rescaled when a row's maximum passes m by more than 8 (log2 units;
 // P <= 256 is exact enough in bf16 and fp32), so the common path never
 // touches O.
@@ -955,14 +955,7 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 64 consecutive 32-bit TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-                 : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
+// 32 consecutive 32-bit TMEM columns of each lane of the warp's quarter.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
                  : "memory");
@@ -970,12 +963,32 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// 32 consecutive 32-bit TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+// Half-split access (shape 16x32bx2): threads 0-15 reach TMEM lanes
+// base+0..15 at columns [c, c+n), threads 16-31 the same lanes at columns
+// [c+n, c+2n).  Two threads thus share one lane (one query row), each with
+// its own half of the row's columns.
+__device__ __forceinline__ void tmem_ld_h32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32], 32;"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
                  : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_h16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16], 16;"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st_h32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%0], 32, {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_h16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], 16, {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
 }
 
 }  // namespace tc
@@ -1022,10 +1035,12 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     using tc::mma_commit;
     using tc::fence_before;
     using tc::fence_after;
-    using tc::tmem_ld64;
-    using tc::tmem_ld32;
     using tc::tmem_st32;
     using tc::tmem_wait_st;
+    using tc::tmem_ld_h32;
+    using tc::tmem_ld_h16;
+    using tc::tmem_st_h32;
+    using tc::tmem_st_h16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1294,6 +1309,17 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         const long long row_w = static_cast<long long>(p.Hq + 2 * p.Hkv) * kD;
         float *normw = reinterpret_cast<float *>(smem + kOffNormW);  // [0..63] q, [64..127] k
         if (QKNORM && t < 2 * kD) normw[t] = __bfloat162float(t < kD ? p.q_w[t] : p.k_w[t - kD]);
+        if (set == 0) {
+            // Rows sit in TMEM lanes 0-11 of each quarter and P is written
+            // below for lanes 0-15 only: zero the P columns of the whole
+            // quarter once so the P.V products of the unused lanes read zeros.
+            uint32_t zero[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) zero[j] = 0u;
+#pragma unroll
+            for (uint32_t c = 0; c < 2u * kPCols; c += 32u) tmem_st32(tmem + lane_off + kColP + c, zero);
+            tmem_wait_st();
+        }
         // A chunk's partial is written while the next chunk's first item is in
         // flight (its P.V, the last O reader, was confirmed just before), so
         // the wait for the chunk's last P.V hides behind that item's softmax.
@@ -1301,9 +1327,9 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         long long epi_slot = 0;
         float epi_m = 0.f, epi_l = 0.f;
         auto write_partial = [&]() {
-            // Set s writes O columns [kDimsPerSet*s, +kDimsPerSet): lane half
-            // 0 the first half of them, half 1 the second, each adding the
-            // partner lane's share (the other half of the keys).
+            // Set s writes O columns [kDimsPerSet*s, +kDimsPerSet) of the
+            // row's one TMEM lane: thread half 0 the first half of them, half
+            // 1 the second.  The row sum adds the two halves' key shares.
             float ltot = epi_l + __shfl_xor_sync(kFull, epi_l, 16);
             if (kSets > 1) {
                 xsum[set * 128 + tl] = ltot;
@@ -1313,18 +1339,14 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                 for (int s2 = 0; s2 < kSets; ++s2) ltot += xsum[s2 * 128 + tl];
             }
             constexpr int kKeep = kDimsPerSet / 2;
-            uint32_t orr[kDimsPerSet];
-#pragma unroll
-            for (int c = 0; c < kDimsPerSet / 32; ++c)
-                tmem_ld32(tmem + lane_off + kColO + kDimsPerSet * set + 32u * c,
-                          *reinterpret_cast<uint32_t(*)[32]>(orr + 32 * c));
+            uint32_t orr[kKeep];
+            if constexpr (kKeep == 32)
+                tmem_ld_h32(tmem + lane_off + kColO + kDimsPerSet * set, *reinterpret_cast<uint32_t(*)[32]>(orr));
+            else
+                tmem_ld_h16(tmem + lane_off + kColO + kDimsPerSet * set, *reinterpret_cast<uint32_t(*)[16]>(orr));
             float outv[kKeep];
 #pragma unroll
-            for (int j = 0; j < kKeep; ++j) {
-                const float give = __uint_as_float(half ? orr[j] : orr[kKeep + j]);
-                const float keep = __uint_as_float(half ? orr[kKeep + j] : orr[j]);
-                outv[j] = keep + __shfl_xor_sync(kFull, give, 16);
-            }
+            for (int j = 0; j < kKeep; ++j) outv[j] = __uint_as_float(orr[j]);
             if (active) {
                 // The partial's O leaves as bf16: half the bytes for the
                 // split pass to write and the combine to read; one rounding
@@ -1407,7 +1429,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                 const int rix = t >> 1, hp = t & 1;
                 const uint8_t *src = nullptr;
                 uint8_t *dst = nullptr;
-                int drow = 0, drow2 = -1, ti = 0;
+                int drow = 0, ti = 0;
                 bool norm = false;
                 const float *w = normw;
                 if (rix < kRows) {
@@ -1417,7 +1439,6 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                         src = raw_q + (ti * kG + g) * 128;
                         dst = qtile;
                         drow = (rix / kRowsPerQuarter) * 32 + rix % kRowsPerQuarter;
-                        drow2 = drow + 16;
                         norm = QKNORM;
                     }
                 } else if (rix < kRows + kMaxB) {
@@ -1484,10 +1505,6 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                     for (int c = 0; c < 2; ++c) {
                         *reinterpret_cast<uint4 *>(dst + swz(drow, 2 * hp + c)) = o[c];
                         *reinterpret_cast<uint4 *>(dst + swz(drow, 4 + 2 * hp + c)) = o[2 + c];
-                        if (drow2 >= 0) {
-                            *reinterpret_cast<uint4 *>(dst + swz(drow2, 2 * hp + c)) = o[c];
-                            *reinterpret_cast<uint4 *>(dst + swz(drow2, 4 + 2 * hp + c)) = o[2 + c];
-                        }
                     }
                 }
             }
@@ -1511,13 +1528,13 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                     }
                     mbar_wait(bar_sfull + 8 * b, static_cast<uint32_t>((it >> 1) & 1), abort_flag, p.status);
                     fence_after();
-                    // This lane's half of the keys of page `set` of the group.
+                    // This thread's half of the keys of page `set` of the group.
                     float sv[32];
                     {
-                        uint32_t sr[64];
-                        tmem_ld64(tmem + lane_off + kSCols * b + 64u * set, sr);
+                        uint32_t sr[32];
+                        tmem_ld_h32(tmem + lane_off + kSCols * b + 64u * set, sr);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(half ? sr[32 + j] : sr[j]);
+                        for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(sr[j]);
                     }
                     if (valid < kKeys) {
                         const int lim = valid - 64 * set - 32 * half;
@@ -1556,15 +1573,9 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                             rs[j & 3] += p0 + p1;
                             pk[j] = pack_bf16(p0, p1);
                         }
-                        // P row of this lane for page `set`: its half of the
-                        // keys, zeros in the other half.
-                        uint32_t prow[32];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            prow[j] = half ? 0u : pk[j];
-                            prow[16 + j] = half ? pk[j] : 0u;
-                        }
-                        tmem_st32(tmem + lane_off + kColP + kPCols * b + 32u * set, prow);
+                        // The row's P for page `set`: this thread's half of
+                        // the keys, 16 columns of bf16 pairs.
+                        tmem_st_h16(tmem + lane_off + kColP + kPCols * b + 32u * set, pk);
                     }
                     lsum = (first ? 0.f : lsum * f) + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
                     m_used = m_new;
@@ -1584,16 +1595,21 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                     }
                     if (epi_pending) write_partial();  // before this item's P.V overwrites O
                     if (__any_sync(kFull, need)) {
-                        // Each set rescales its own O columns.
+                        // Each set rescales its own O columns of the row,
+                        // the two thread halves one half of them each.
+                        const uint32_t col = tmem + lane_off + kColO + kDimsPerSet * set;
+                        constexpr int kHalf = kDimsPerSet / 2;
+                        uint32_t part[kHalf];
+                        if constexpr (kHalf == 32)
+                            tmem_ld_h32(col, *reinterpret_cast<uint32_t(*)[32]>(part));
+                        else
+                            tmem_ld_h16(col, *reinterpret_cast<uint32_t(*)[16]>(part));
 #pragma unroll
-                        for (int c = 0; c < kDimsPerSet / 32; ++c) {
-                            const uint32_t col = tmem + lane_off + kColO + kDimsPerSet * set + 32u * c;
-                            uint32_t part[32];
-                            tmem_ld32(col, part);
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) part[j] = __float_as_uint(__uint_as_float(part[j]) * f);
-                            tmem_st32(col, part);
-                        }
+                        for (int j = 0; j < kHalf; ++j) part[j] = __float_as_uint(__uint_as_float(part[j]) * f);
+                        if constexpr (kHalf == 32)
+                            tmem_st_h32(col, *reinterpret_cast<uint32_t(*)[32]>(part));
+                        else
+                            tmem_st_h16(col, *reinterpret_cast<uint32_t(*)[16]>(part));
                         tmem_wait_st();
                     }
                     if (is_page && (valid & (kP - 1)) != 0) {

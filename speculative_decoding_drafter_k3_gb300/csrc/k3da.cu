@@ -891,20 +891,23 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // Shared memory (offsets from a 1024-byte aligned base).
 constexpr int kOffStages = 0;                        // kStages x kGroupBytes
 constexpr int kOffQ = kStages * kGroupBytes;         // 128 rows x 128 B, 128B swizzle
-constexpr int kOffBlkK = kOffQ + 128 * 128;          // 64 rows x 128 B
-constexpr int kOffBlkV = kOffBlkK + 64 * 128;        // 64 rows x 128 B
-constexpr int kOffRaw = kOffBlkV + 64 * 128;         // raw q [8][6][64], k [8][64], v [8][64]
+constexpr int kBlkRows = 16;                          // block tiles: B <= 8 keys, one 16-row MMA step
+constexpr int kOffBlkK = kOffQ + 128 * 128;          // kBlkRows rows x 128 B
+constexpr int kOffBlkV = kOffBlkK + kBlkRows * 128;  // kBlkRows rows x 128 B
+constexpr int kOffRaw = kOffBlkV + kBlkRows * 128;   // raw q [8][6][64], k [8][64], v [8][64]
 constexpr int kOffTrig = kOffRaw + kMaxB * (kG + 2) * kD * 2;  // [8][32] float2
-constexpr int kOffNormW = kOffTrig + kMaxB * 32 * 8;  // q and k norm weights, [2][64] float
-constexpr int kOffXch = kOffNormW + 2 * kD * 4;      // row max [2][kSets][128], row sum [kSets][128]
-constexpr int kOffPlan = kOffXch + 3 * kSets * 128 * 4;
+constexpr int kOffNormW = kOffTrig + kMaxB * 32 * 8;  // q and k norm weights, [2][64] bf16
+constexpr int kOffXch = kOffNormW + 2 * kD * 2;      // row max [2][kSets][128], row sum [kSets][128]
+constexpr int kOffPlan = kOffXch + (kSets > 1 ? 3 * kSets * 128 * 4 : 0);  // one set exchanges nothing
 constexpr int kNumBars = 2 * kStages + 8;  // full, empty, s_full[2], p_full[2], o_done[2], q_ready, done
-constexpr int kOffBar = kOffPlan + 1536;
+constexpr int kOffBar = kOffPlan + (static_cast<int>(sizeof(Plan)) + 15) / 16 * 16;
 constexpr int kOffTaddr = kOffBar + kNumBars * 8;
 constexpr int kOffFlag = kOffTaddr + 8;
 constexpr int kSmemUsed = kOffFlag + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+// Two CTAs per SM: 228 KB per SM, 1 KB of it reserved per CTA.
+static_assert(kCtasPerSm == 1 || 2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs fit an SM's shared memory");
 static_assert(kOffQ % 1024 == 0 && kOffBlkK % 1024 == 0 && kOffBlkV % 1024 == 0, "SW128 tiles need 1 KB alignment");
 static_assert(kOffBar % 8 == 0 && kOffPlan % 8 == 0, "mbarrier / int64 alignment");
 
@@ -915,7 +918,7 @@ constexpr uint32_t idesc_f16(uint32_t m, uint32_t n, bool b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? 1u << 16 : 0u) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 constexpr uint32_t kIdescQK = idesc_f16(128, 64 * kGroup, false);  // a page group's keys
-constexpr uint32_t kIdescQKBlock = idesc_f16(128, 64, false);       // the block tile
+constexpr uint32_t kIdescQKBlock = idesc_f16(128, kBlkRows, false); // the block tile
 constexpr uint32_t kIdescPV = idesc_f16(128, 64, true);
 
 // Shared-memory matrix descriptor of a tile stored in 128-byte rows with the
@@ -1017,6 +1020,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     constexpr auto kOffQ = tc::kOffQ;
     constexpr auto kOffBlkK = tc::kOffBlkK;
     constexpr auto kOffBlkV = tc::kOffBlkV;
+    constexpr auto kBlkRows = tc::kBlkRows;
     constexpr auto kOffRaw = tc::kOffRaw;
     constexpr auto kOffTrig = tc::kOffTrig;
     constexpr auto kOffNormW = tc::kOffNormW;
@@ -1058,7 +1062,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         // Q and block tiles start as zeros: rows without a query row or a
         // block token stay zero for the whole kernel.
         uint4 *z = reinterpret_cast<uint4 *>(smem + kOffQ);
-        for (int e = threadIdx.x; e < (128 * 128 + 2 * 64 * 128) / 16; e += kThreads) z[e] = make_uint4(0, 0, 0, 0);
+        for (int e = threadIdx.x; e < (128 * 128 + 2 * kBlkRows * 128) / 16; e += kThreads) z[e] = make_uint4(0, 0, 0, 0);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (threadIdx.x == 0) {
@@ -1307,8 +1311,8 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         float *xmax = reinterpret_cast<float *>(smem + kOffXch);  // [2][kSets][128]
         float *xsum = xmax + 2 * kSets * 128;                      // [kSets][128]
         const long long row_w = static_cast<long long>(p.Hq + 2 * p.Hkv) * kD;
-        float *normw = reinterpret_cast<float *>(smem + kOffNormW);  // [0..63] q, [64..127] k
-        if (QKNORM && t < 2 * kD) normw[t] = __bfloat162float(t < kD ? p.q_w[t] : p.k_w[t - kD]);
+        __nv_bfloat16 *normw = reinterpret_cast<__nv_bfloat16 *>(smem + kOffNormW);  // [0..63] q, [64..127] k
+        if (QKNORM && t < 2 * kD) normw[t] = t < kD ? p.q_w[t] : p.k_w[t - kD];
         if (set == 0) {
             // Rows sit in TMEM lanes 0-11 of each quarter and P is written
             // below for lanes 0-15 only: zero the P columns of the whole
@@ -1431,7 +1435,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                 uint8_t *dst = nullptr;
                 int drow = 0, ti = 0;
                 bool norm = false;
-                const float *w = normw;
+                const __nv_bfloat16 *w = normw;
                 if (rix < kRows) {
                     if (rix < rows) {
                         const int g = rix / p.B;
@@ -1485,8 +1489,8 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const int jp = 16 * hp + e;
-                        const float n_lo = lo[e] * inv * w[jp];
-                        const float n_hi = hi[e] * inv * w[jp + 32];
+                        const float n_lo = lo[e] * inv * __bfloat162float(w[jp]);
+                        const float n_hi = hi[e] * inv * __bfloat162float(w[jp + 32]);
                         const float2 cs = trig[ti * 32 + jp];
                         lo[e] = n_lo * cs.x - n_hi * cs.y;
                         hi[e] = n_hi * cs.x + n_lo * cs.y;

@@ -2,7 +2,8 @@
 """Benchmark of the K3 DFlash drafter block attention; prints ONE JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload long_context|mixed_8x8|heads_24_4|tiny]
+                    [--workload long_context|mixed_8x8|heads_24_4|tiny|w6_8x6|single_w6|...]
+                    [--yarn] [--op attn|qk_norm_rope] [--warm-l2] [--no-e2e] [--no-cpu-baseline]
 
 Metric: drafter block-attention microseconds per call (lower is better) on
 one of the op's workloads, default the long-context one (8 requests x 8 draft
@@ -16,7 +17,10 @@ ours:       the CUDA library through its Python binding.  Inputs are resident
             launching stream.  "e2e" times the same call with the per-step
             inputs (qkv, page table, lengths, positions) copied from pinned
             host memory in one packed copy and the output copied back, inside
-            the timed region.
+            the timed region.  --warm-l2 skips the flush (a warm-cache line,
+            labelled in "config").  "cpu_baseline" is the fp64 oracle on one
+            host thread (a bounded sample scaled to a call); "cpu_all_cores"
+            is one whole call of it on all host cores.
 reference:  the fp64 CPU oracle (test infrastructure, timed as it stands on
             the host cores), each step a bounded sample of the same workload
             scaled to a whole call.
@@ -66,6 +70,9 @@ def parse():
     ap.add_argument("--heads", choices=["6/1", "24/4"], default="24/4")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--warm-l2", action="store_true",
+                    help="do not flush L2 between timed calls (a labelled warm-cache line, "
+                         "never the headline)")
     return ap.parse_args()
 
 
@@ -240,6 +247,59 @@ def cpu_baseline(case, budget_s: float = 12.0):
                        f"scaled to one call by token count")}
 
 
+def compact_unit(case, r, h):
+    """The (request r, kv head h) unit alone as numpy arrays for the oracle:
+    its q heads, k head and v head of qkv and that kv head of the request's
+    pages (input marshalling only)."""
+    import oracle
+
+    sub = compact_request(case, r)
+    G, D = case.Hq // case.Hkv, case.D
+    heads = list(range(h * G, (h + 1) * G)) + [case.Hq + h, case.Hq + case.Hkv + h]
+    qkv = sub.qkv.view(case.B, case.Hq + 2 * case.Hkv, D)[:, heads].reshape(case.B, (G + 2) * D)
+    pool = sub.pool[:, :, h:h + 1].contiguous()
+    unit = {"qkv": oracle.bf16_bits(qkv), "pool": oracle.bf16_bits(pool),
+            "page_table": sub.page_table.numpy(), "ctx_lens": sub.ctx_lens.numpy(),
+            "G": G, "B": case.B, "scale": case.scale, "qknorm": case.qknorm,
+            "tokens": sub.lens_list()[0] + case.B}
+    if case.qknorm:
+        unit.update(positions=sub.positions.numpy(), q_norm_w=oracle.bf16_bits(sub.q_norm_w),
+                    k_norm_w=oracle.bf16_bits(sub.k_norm_w), eps=case.eps, rope_base=case.rope_base)
+    return unit
+
+
+def _oracle_unit(u):
+    import oracle
+
+    return oracle.attn(u["qkv"], u["pool"], u["page_table"], u["ctx_lens"], num_requests=1, block_len=u["B"],
+                num_q_heads=u["G"], num_kv_heads=1, scale=u["scale"], qknorm=u["qknorm"],
+                positions=u.get("positions"), q_norm_w=u.get("q_norm_w"), k_norm_w=u.get("k_norm_w"),
+                eps=u.get("eps", 1e-5), rope_base=u.get("rope_base", 10000.0))
+
+
+def cpu_all_cores(case, threads: int = 0):
+    """One whole call of the oracle on all host cores: the R x Hkv
+    independent (request, kv head) units, longest first, on a pool of
+    threads (the C oracle keeps no global state and ctypes releases the GIL
+    during each call).  Wall-clock time of the pool; inputs marshalled
+    before the clock starts."""
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+
+    oracle.build()
+    n = threads or len(os.sched_getaffinity(0))
+    units = sorted((compact_unit(case, r, h) for r in range(case.R) for h in range(case.Hkv)),
+                   key=lambda u: -u["tokens"])
+    with ThreadPoolExecutor(max_workers=n) as ex:
+        list(ex.map(lambda _: None, range(n)))  # threads started before the clock
+        t0 = time.perf_counter()
+        list(ex.map(_oracle_unit, units))
+        wall = time.perf_counter() - t0
+    return {"value": wall * 1e6, "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": (f"fp64 C oracle, one whole call: {len(units)} (request, kv head) units on "
+                       f"{n} threads, wall clock")}
+
+
 # ------------------------------------------------------------------ arms --
 
 def config_of(case, extra=None):
@@ -305,6 +365,8 @@ def run_ours(args, world, rank):
             # Write a buffer larger than L2, then read another one: L2 ends
             # up holding clean lines of neither input, so the timed call
             # neither hits in L2 nor pays for writing back the flush.
+            if args.warm_l2:
+                return
             flush_w.zero_()
             torch.sum(flush_r, dim=0, out=sink)
 
@@ -422,6 +484,8 @@ def run_ours(args, world, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",
             "data": "synthetic (seeded N(0,1) bf16 pool/qkv, random page permutation)",
             "config": config_of(case, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                                       **({"l2": "warm: not flushed between timed calls (inputs stay "
+                                                 "in L2 from the previous call)"} if args.warm_l2 else {}),
                                        "rope": "yarn(4.0, 4096, 32, 1)" if yarn is not None else "neox",
                                        "split_ctas": k3da.split_grid(dev.index)}),
             "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clock_info,
@@ -430,6 +494,7 @@ def run_ours(args, world, rank):
                                 sorted(call_ms)[int(0.9 * (K - 1))] * 1e3]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case)
+        line["cpu_all_cores"] = cpu_all_cores(case)
     if rank == 0:
         print(json.dumps(line), flush=True)
 

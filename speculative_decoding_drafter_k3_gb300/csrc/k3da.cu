@@ -1294,13 +1294,13 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         const int t = threadIdx.x;
         const int q = warp & 3;
         const int set = warp >> 2;
-        const int half = lane >> 4;               // key half of this lane
+        const int half = lane >> 4;               // key half of this thread
         const int l16 = lane & 15;
         const int rho = l16 < kRowsPerQuarter ? q * kRowsPerQuarter + l16 : 1 << 20;
         const int rows = kG * p.B;
         const bool active = rho < rows;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
-        const int tl = 32 * q + lane;             // TMEM lane of this thread
+        const int tl = 32 * q + lane;             // exchange slot of this thread (row, key half)
         uint8_t *qtile = smem + kOffQ;
         uint8_t *bk = smem + kOffBlkK;
         uint8_t *bv = smem + kOffBlkV;

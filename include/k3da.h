@@ -84,7 +84,8 @@ size_t k3da_workspace_bytes(int num_requests, int block_len, int num_q_heads,
  *   page_table   [R, page_stride] int32; context token c of request r is in
  *                page page_table[r*page_stride + c/64], slot c%64.  Entries
  *                past ceil(ctx_len/64) are never read.
- *   page_stride  entries per page-table row, >= 1.
+ *   page_stride  entries per page-table row, 1 .. 2^25 - 1 (so that
+ *                page_stride * 64 fits an int).
  *   ctx_lens     [R] int32 context lengths, 0 <= len <= page_stride*64.
  *   num_requests R in [1, 8];  block_len B in [1, 8].
  *   num_q_heads, num_kv_heads   (6, 1) or (24, 4); query head h reads KV
@@ -100,6 +101,17 @@ size_t k3da_workspace_bytes(int num_requests, int block_len, int num_q_heads,
  * Returns K3DA_OK once both kernels are enqueued, else a k3da_error.
  * Calls on the same stream are ordered; calls that share a workspace must
  * not overlap on the GPU.
+ *
+ * Work split and reproducibility.  Each (request, kv head) unit's keys are
+ * cut into chunks whose boundaries depend only on that unit's context length
+ * and on the call's shape (R, Hkv): at most 32 pages per chunk, and with few
+ * units about 304 chunks in all (two per SM of a 152-SM GB300) so that even
+ * one request spreads over the GPU.  That count is a constant, not the
+ * device's SM count, and the chunk partials are folded in a fixed order: the
+ * output is bitwise the same on every run, whatever the other requests hold
+ * (requests are isolated bit for bit), and on any device this library runs
+ * on, whatever its SM count (which only decides which CTA computes which
+ * chunk).
  */
 int k3da_attn(void *out, const void *qkv, const void *kv_pool, int64_t num_pages,
               const int32_t *page_table, int page_stride, const int32_t *ctx_lens,
@@ -192,17 +204,18 @@ int k3da_split_grid(int device);
  * with r_j = original_max_position * theta_j / (2 pi) (its wavelengths in the
  * original context) and the ramp g = clamp((r_j - beta_slow) / (beta_fast -
  * beta_slow), 0, 1), it turns at g * theta_j + (1 - g) * theta_j / factor.
- * Both rotated outputs are multiplied by mscale (the YaRN paper's sqrt(1/t), i.e.
- * 0.1 * ln(factor) + 1, applied to q and k; pass 1 when the model folds it
- * elsewhere).  factor 1 with mscale 1 is plain NeoX RoPE.  Host memory; read
- * during the call only.
+ * Both rotated outputs are multiplied by mscale (the YaRN paper's sqrt(1/t),
+ * applied to q and k; pass 1 when the model folds it elsewhere, or 0 to have
+ * the library use the paper's 0.1 * ln(factor) + 1, formed in fp64 and
+ * rounded once to fp32).  factor 1 with mscale 1 is plain NeoX RoPE.  Host
+ * memory; read during the call only.
  */
 typedef struct {
     float factor;                /* >= 1 */
     float original_max_position; /* > 0 */
     float beta_fast;             /* > beta_slow (32 in the YaRN paper) */
     float beta_slow;             /* > 0 (1 in the YaRN paper) */
-    float mscale;                /* > 0 */
+    float mscale;                /* > 0, or 0 for 0.1 * ln(factor) + 1 */
 } k3da_yarn;
 
 /*

@@ -34,9 +34,6 @@
 //     with one batch of cp.async copies and turned into operand tiles:
 //     RMSNorm and RoPE happen on the way in, RoPE angles are reduced in fp64
 //     then turned by an accurate sincosf.
-//   * k3da_split_kernel, the first design (6 consumer warps with mma.sync
-//     m16n8k16 and ldmatrix, + 1 producer warp), is kept as the
-//     legacy-tensor-core baseline: built with -DK3DA_USE_TCGEN05=0.
 //   * Each chunk leaves an unnormalised partial (O as bf16, m and l in fp32)
 //     in the workspace; the combine kernel folds a unit's chunk partials in
 //     a fixed order and writes bf16 out, so reruns are bit-identical.
@@ -63,42 +60,16 @@ constexpr int kRows = 48;        // kG * max block length
 constexpr int kMaxR = 8;
 constexpr int kMaxB = 8;
 constexpr int kMaxUnits = 32;    // 8 requests x 4 kv heads
-constexpr int kRowWarps = 3;      // 16 query rows each
-constexpr int kKeyGroups = 2;     // each page's 64 keys split in two halves
-constexpr int kConsumerWarps = kRowWarps * kKeyGroups;
-constexpr int kConsumerThreads = 32 * kConsumerWarps;
-constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kTileBytes = kP * kD * 2;       // 8 KB: one page, one head, K or V
 constexpr int kStageBytes = 2 * kTileBytes;   // K + V
-#ifndef K3DA_STAGES
-#define K3DA_STAGES 4
-#endif
-constexpr int kStages = K3DA_STAGES;
 constexpr int kMaxCtasPerSm = 2;
 constexpr int kChunkSplits = 16;   // a unit is cut into at most this many chunks ...
 constexpr int kChunkTarget = 304;  // ... or, with few units, about this many chunks in all
-#ifndef K3DA_CHUNK_MAX
-#define K3DA_CHUNK_MAX 32
-#endif
-constexpr int kChunkMax = K3DA_CHUNK_MAX;  // ... of at most this many pages, beyond which it gets more chunks
+constexpr int kChunkMax = 32;      // ... of at most this many pages, beyond which it gets more chunks
 constexpr int kPartialElems = kRows * kD;     // O of one chunk, bf16
+constexpr int kMaxPageStride = 0x7fffffff / kP;  // page_stride * 64 stays an int
 constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
-
-// Shared-memory layout (offsets from a 1024-byte aligned base).
-[[maybe_unused]] constexpr int kOffStages = 0;
-constexpr int kOffQ = kStages * kStageBytes;          // 48 rows x 128 B
-constexpr int kOffBlkK = kOffQ + kRows * 128;         // 16 rows x 128 B
-constexpr int kOffBlkV = kOffBlkK + 16 * 128;
-constexpr int kOffRaw = kOffBlkV + 16 * 128;          // raw q [8][6][64], k [8][64], v [8][64]
-constexpr int kOffTrig = kOffRaw + kMaxB * (kG + 2) * kD * 2;  // [8][32] float2
-constexpr int kOffMerge = kOffTrig + kMaxB * 32 * 8;  // [3][36][32] float
-constexpr int kOffPlan = kOffMerge + kRowWarps * 36 * 32 * 4;  // struct Plan
-constexpr int kOffBar = kOffPlan + 1536;              // 2*kStages mbarriers
-constexpr int kOffFlag = kOffBar + 2 * kStages * 8;
-constexpr int kSmemUsed = kOffFlag + 16;
-[[maybe_unused]] constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for alignment
-static_assert(kOffBar % 8 == 0 && kOffPlan % 8 == 0, "mbarrier / int64 alignment");
 
 struct Params {
     __nv_bfloat16 *out;
@@ -197,29 +168,6 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-[[maybe_unused]] __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                        uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-[[maybe_unused]] __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                          uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-[[maybe_unused]] __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 // 2^x on the SFU (ex2.approx, flush to zero; 2^-inf = +0).
 __device__ __forceinline__ float exp2_approx(float x) {
     float y;
@@ -273,13 +221,9 @@ __host__ __device__ constexpr int chunk_splits(int units) {
 }
 
 // Warp 0 reads and checks ctx_lens and builds the plan, one lane per unit
-// with shuffle scans; cta < 0 builds only the unit tables (for the
-// combine).  The caller syncs.  An item is the block (item 0) or a group of
-// G consecutive pages of the unit (the last group may be shorter); a chunk
-// holds at most kChunkMax / G items.
-template <int G>
+// with shuffle scans.  The caller syncs.  An item is the block (item 0) or
+// one page of the unit; a chunk holds at most kChunkMax items.
 __device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool report) {
-    constexpr int kChunkItems = kChunkMax / G > 0 ? kChunkMax / G : 1;
     if (threadIdx.x >= 32) return;
     const int lane = threadIdx.x;
     int L = 0;
@@ -299,7 +243,7 @@ __device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool repor
     const int splits = chunk_splits(U);
     if (u < U) {
         npages = (Lu + kP - 1) / kP;
-        items = 1 + (npages + G - 1) / G;
+        items = 1 + npages;
         // Finer chunks for few units, but never below the 16-way split's
         // chunk or 4 items, whichever is smaller: short units keep the
         // chunking of the 16-way split.
@@ -307,7 +251,7 @@ __device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool repor
         const int ch16 = (items + kChunkSplits - 1) / kChunkSplits;
         const int floor_ch = ch16 < 4 ? ch16 : 4;
         ch = ch > floor_ch ? ch : floor_ch;
-        ch = ch < 1 ? 1 : (ch > kChunkItems ? kChunkItems : ch);
+        ch = ch < 1 ? 1 : (ch > kChunkMax ? kChunkMax : ch);
         nch = (items + ch - 1) / ch;
     }
     long long si = items;  // inclusive scans over units
@@ -349,8 +293,8 @@ __device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool repor
             j1 = static_cast<int>(b);
             const int i0 = j0 * ch;
             const int i1 = j1 * ch < items ? j1 * ch : items;
-            p0 = i0 == 0 ? 0 : (i0 - 1) * G;
-            const int pe = (i1 - 1) * G < npages ? (i1 - 1) * G : npages;
+            p0 = i0 == 0 ? 0 : i0 - 1;
+            const int pe = i1 - 1;
             npg = pe - p0;
         }
     }
@@ -372,151 +316,6 @@ __device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool repor
     if (lane == 0) pl->nrun = __popc(mask);
 }
 
-// ------------------------------------------------------------- consumers --
-
-struct RowState {
-    float m[2];   // running max (log2 units) of rows a = lane/4 and b = a + 8
-    float l[2];   // running sum (this lane's share of the row)
-    float o[8][4];
-};
-
-// Attend the warp's 16 query rows to NT*8 keys of a staged tile: K rows and
-// V rows key0 .. key0 + NT*8 - 1 of the tiles at kbase / vbase (128-byte
-// swizzled).  valid (>= 1) = how many of those keys are real; the rest are
-// masked out of the softmax and their values zeroed.
-template <int NT>
-__device__ __forceinline__ void attend_tile(RowState &st, const uint32_t (&qf)[4][4],
-                                            uint32_t kbase, uint32_t vbase, int key0, int valid,
-                                            float scale_log2, int lane) {
-    static_assert(NT % 2 == 0, "keys come in 16-key steps");
-    float s[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-    const int mi = lane >> 3, rr = lane & 7;
-    // S = Q K^T; B operand = K rows (keys) with dims contiguous.
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-        for (int kk2 = 0; kk2 < 2; ++kk2) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(kbase + swz(key0 + nt * 8 + rr, kk2 * 4 + mi), b0, b1, b2, b3);
-            mma_bf16(s[nt], qf[2 * kk2], b0, b1);
-            mma_bf16(s[nt], qf[2 * kk2 + 1], b2, b3);
-        }
-    }
-    const int kq = 2 * (lane & 3);
-    const bool partial = valid < NT * 8;
-    if (partial) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int key = nt * 8 + kq;
-            if (key >= valid) { s[nt][0] = -INFINITY; s[nt][2] = -INFINITY; }
-            if (key + 1 >= valid) { s[nt][1] = -INFINITY; s[nt][3] = -INFINITY; }
-        }
-    }
-    // Online softmax in base 2 with the scale folded into the exponent.
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        mx[0] = fmaxf(mx[0], fmaxf(s[nt][0], s[nt][1]));
-        mx[1] = fmaxf(mx[1], fmaxf(s[nt][2], s[nt][3]));
-    }
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        mx[e] = fmaxf(mx[e], __shfl_xor_sync(kFull, mx[e], 1));
-        mx[e] = fmaxf(mx[e], __shfl_xor_sync(kFull, mx[e], 2));
-    }
-    float mnew[2], alpha[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        mnew[e] = fmaxf(st.m[e], mx[e] * scale_log2);
-        alpha[e] = exp2_approx(st.m[e] - mnew[e]);
-        st.m[e] = mnew[e];
-    }
-    float rs[2] = {0.f, 0.f};
-    uint32_t pf[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const float p0 = exp2_approx(fmaf(s[nt][0], scale_log2, -mnew[0]));
-        const float p1 = exp2_approx(fmaf(s[nt][1], scale_log2, -mnew[0]));
-        const float p2 = exp2_approx(fmaf(s[nt][2], scale_log2, -mnew[1]));
-        const float p3 = exp2_approx(fmaf(s[nt][3], scale_log2, -mnew[1]));
-        rs[0] += p0 + p1;
-        rs[1] += p2 + p3;
-        pf[nt][0] = pack_bf16(p0, p1);
-        pf[nt][1] = pack_bf16(p2, p3);
-    }
-#pragma unroll
-    for (int e = 0; e < 2; ++e) st.l[e] = st.l[e] * alpha[e] + rs[e];
-#pragma unroll
-    for (int nd = 0; nd < 8; ++nd) {
-        st.o[nd][0] *= alpha[0];
-        st.o[nd][1] *= alpha[0];
-        st.o[nd][2] *= alpha[1];
-        st.o[nd][3] *= alpha[1];
-    }
-    // O += P V: A operand = P straight from the score registers; B operand =
-    // V rows (keys) read transposed.
-#pragma unroll
-    for (int kk = 0; kk < NT / 2; ++kk) {
-        const uint32_t a[4] = {pf[2 * kk][0], pf[2 * kk][1], pf[2 * kk + 1][0], pf[2 * kk + 1][1]};
-        uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
-        if (partial) {
-            // Values of masked keys are zeroed so that stale non-finite pool
-            // contents cannot reach the accumulator (0 * inf).
-            const int k0 = kk * 16 + kq;
-            keep_lo = ((k0 < valid) ? 0x0000ffffu : 0u) | ((k0 + 1 < valid) ? 0xffff0000u : 0u);
-            keep_hi = ((k0 + 8 < valid) ? 0x0000ffffu : 0u) | ((k0 + 9 < valid) ? 0xffff0000u : 0u);
-        }
-#pragma unroll
-        for (int ndp = 0; ndp < 4; ++ndp) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(vbase + swz(key0 + kk * 16 + (mi & 1) * 8 + rr, ndp * 2 + (mi >> 1)), b0, b1, b2,
-                      b3);
-            if (partial) {
-                b0 &= keep_lo;
-                b2 &= keep_lo;
-                b1 &= keep_hi;
-                b3 &= keep_hi;
-            }
-            mma_bf16(st.o[2 * ndp], a, b0, b1);
-            mma_bf16(st.o[2 * ndp + 1], a, b2, b3);
-        }
-    }
-}
-
-// RMSNorm (QKNORM) and NeoX RoPE (QKNORM) of one 64-wide head row whose
-// dims lane and lane + 32 are x_lo, x_hi; writes the bf16 result into row
-// `row` of a swizzled tile.  w_lo / w_hi are the norm weights of those dims.
-template <bool QKNORM>
-__device__ __forceinline__ void prep_row(uint8_t *tile, int row, float x_lo, float x_hi, float w_lo,
-                                         float w_hi, float eps, float2 cs, int lane, int row2 = -1) {
-    float y_lo = x_lo, y_hi = x_hi;
-    if (QKNORM) {
-        float ss = x_lo * x_lo + x_hi * x_hi;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
-        const float inv = rsqrtf(ss * (1.0f / kD) + eps);
-        const float n_lo = x_lo * inv * w_lo;
-        const float n_hi = x_hi * inv * w_hi;
-        y_lo = n_lo * cs.x - n_hi * cs.y;
-        y_hi = n_hi * cs.x + n_lo * cs.y;
-    }
-    const __nv_bfloat16 b_lo = __float2bfloat16_rn(y_lo), b_hi = __float2bfloat16_rn(y_hi);
-    *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, lane >> 3) + (lane & 7) * 2) = b_lo;
-    *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, 4 + (lane >> 3)) + (lane & 7) * 2) = b_hi;
-    if (row2 >= 0) {
-        *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row2, lane >> 3) + (lane & 7) * 2) = b_lo;
-        *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row2, 4 + (lane >> 3)) + (lane & 7) * 2) = b_hi;
-    }
-}
-
-[[maybe_unused]] __device__ __forceinline__ void zero_row(uint8_t *tile, int row, int lane) {
-    const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
-    *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, lane >> 3) + (lane & 7) * 2) = z;
-    *reinterpret_cast<__nv_bfloat16 *>(tile + swz(row, 4 + (lane >> 3)) + (lane & 7) * 2) = z;
-}
-
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -525,330 +324,20 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-[[maybe_unused]] __device__ __forceinline__ float bf16_at(const uint8_t *base, int index) {
-    return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[index]);
-}
-
-// ------------------------------------------------------------ split pass --
-//
-// Warps 0..5 consume, warp 6 produces.  Consumer warp w works on query rows
-// 16*(w % 3) .. +15 (row = g*B + i for q head 6h + g, token i) and on keys
-// 32*(w / 3) .. +31 of every staged page (key group w / 3); the two key
-// groups keep separate softmax states and merge at the end of each chunk.
-
-template <bool QKNORM>
-__global__ void __launch_bounds__(kThreads, 2)
-    k3da_split_kernel(const __grid_constant__ CUtensorMap pool_map, const __grid_constant__ Params p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Plan *pl = reinterpret_cast<Plan *>(smem + kOffPlan);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffFlag);
-    const uint32_t bar_full = smem_u32(smem + kOffBar);
-    const uint32_t bar_empty = bar_full + kStages * 8;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    build_plan<1>(p, pl, blockIdx.x, p.grid, blockIdx.x == 0);
-    if (threadIdx.x == 0) {
-        *abort_flag = 0;
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, kConsumerWarps);
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-    const int nrun = pl->nrun;
-    if (blockIdx.x == 0 && threadIdx.x < p.R * p.Hkv) {
-        p.ws_units[threadIdx.x] = pl->cstart[threadIdx.x];
-        p.ws_units[kMaxUnits + threadIdx.x] = pl->nch[threadIdx.x];
-    }
-    if (nrun == 0) {
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        return;
-    }
-
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------ producer warp --
-        // The CTA's pages, run after run, form one sequence; lane l resolves
-        // entry base + l of each 32-entry batch (page id -> TMA row of its K
-        // tile, -1 if out of range), one batch ahead of the loads it feeds.
-        uint64_t policy;
-        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
-        const int total = pl->run_pq[nrun];
-        auto resolve = [&](int q) -> int {
-            if (q >= total) return -1;
-            int k = 0;
-            while (pl->run_pq[k + 1] <= q) ++k;
-            const int u = pl->run_u[k];
-            const int r = u / p.Hkv, h = u - r * p.Hkv;
-            const int page = __ldg(p.page_table + static_cast<long long>(r) * p.page_stride + pl->run_p0[k] +
-                                   (q - pl->run_pq[k]));
-            if (page < 0 || page >= p.num_pages) return -1;  // served as zeros, flagged
-            return ((page * 2 + 0) * p.Hkv + h) * kP;
-        };
-        int next = resolve(lane);
-        for (int base = 0; base < total; base += 32) {
-            const int rows_k = next;
-            next = resolve(base + 32 + lane);
-            const int cnt = total - base < 32 ? total - base : 32;
-            for (int j = 0; j < cnt; ++j) {
-                const long long k = base + j;
-                const int krow = __shfl_sync(kFull, rows_k, j);
-                const int s = static_cast<int>(k % kStages);
-                const uint32_t par = static_cast<uint32_t>((k / kStages) & 1);
-                mbar_wait(bar_empty + 8 * s, par ^ 1u, abort_flag, p.status);
-                uint8_t *stage = smem + kOffStages + s * kStageBytes;
-                if (krow >= 0) {
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
-                        tma_load_tile(smem_u32(stage), &pool_map, krow, bar_full + 8 * s, policy);
-                        tma_load_tile(smem_u32(stage + kTileBytes), &pool_map, krow + p.Hkv * kP,
-                                      bar_full + 8 * s, policy);
-                    }
-                } else {
-                    // Out-of-range page id: flag it and serve zeros.
-                    if (lane == 0 && p.status) atomicOr(p.status, K3DA_STATUS_BAD_PAGE);
-                    uint4 *dst = reinterpret_cast<uint4 *>(stage);
-                    for (int q = lane; q < kStageBytes / 16; q += 32) dst[q] = make_uint4(0, 0, 0, 0);
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_full + 8 * s);
-                }
-                __syncwarp();
-            }
-        }
-        // Drain: every issued load must land before the CTA exits (matters
-        // only when a wait gave up and the consumers stopped early).
-        if (*abort_flag) {
-            for (long long j = (total > kStages ? total - kStages : 0); j < total; ++j) {
-                const int s = static_cast<int>(j % kStages);
-                const uint32_t par = static_cast<uint32_t>((j / kStages) & 1);
-                const unsigned long long t0 = global_ns();
-                while (!mbar_try_wait(bar_full + 8 * s, par) && global_ns() - t0 < kWaitLimitNs) {
-                }
-            }
-        }
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        return;
-    }
-
-    // ------------------------------------------------------ consumer warps --
-    const int ctid = threadIdx.x;            // 0 .. kConsumerThreads-1
-    const int rb = warp % kRowWarps;         // query row block
-    const int grp = warp / kRowWarps;        // key group
-    uint8_t *qtile = smem + kOffQ;
-    uint8_t *bk = smem + kOffBlkK;
-    uint8_t *bv = smem + kOffBlkV;
-    uint8_t *raw_q = smem + kOffRaw;                  // [B][6][64] bf16
-    uint8_t *raw_k = raw_q + kMaxB * kG * kD * 2;     // [B][64]
-    uint8_t *raw_v = raw_k + kMaxB * kD * 2;          // [B][64]
-    float2 *trig = reinterpret_cast<float2 *>(smem + kOffTrig);
-    float *merge = reinterpret_cast<float *>(smem + kOffMerge);
-    const int rows = kG * p.B;
-    const bool active = rb * 16 < rows;
-    const long long row_w = static_cast<long long>(p.Hq + 2 * p.Hkv) * kD;
-    const int mi = lane >> 3, rr = lane & 7;
-    float wq_lo = 1.f, wq_hi = 1.f, wk_lo = 1.f, wk_hi = 1.f;
-    if (QKNORM) {
-        wq_lo = __bfloat162float(p.q_w[lane]);
-        wq_hi = __bfloat162float(p.q_w[lane + 32]);
-        wk_lo = __bfloat162float(p.k_w[lane]);
-        wk_hi = __bfloat162float(p.k_w[lane + 32]);
-    }
-    long long k = 0;  // pages consumed
-    for (int run = 0; run < nrun; ++run) {
-        const int u = pl->run_u[run];
-        const int r = u / p.Hkv, h = u - r * p.Hkv;
-        const int L = pl->lens[r];
-        const int ch = pl->ch[u];
-        const int items = static_cast<int>(pl->ustart[u + 1] - pl->ustart[u]);
-        const int j0 = pl->run_j0[run], j1 = pl->run_j1[run];
-        const bool with_block = j0 == 0;
-
-        // ---- stage this unit's q (and block k, v) rows: one round trip.
-        named_bar_sync(1, kConsumerThreads);  // every tile of the previous run is free
-        const char *qkv_rows = reinterpret_cast<const char *>(p.qkv) + static_cast<long long>(r) * p.B * row_w * 2;
-        for (int e = ctid; e < p.B * 48; e += kConsumerThreads) {
-            const int ti = e / 48, c = e - ti * 48;
-            cp_async16(smem_u32(raw_q) + ti * 768 + c * 16,
-                       qkv_rows + ti * row_w * 2 + static_cast<long long>(h) * 768 + c * 16);
-        }
-        if (with_block) {
-            for (int e = ctid; e < p.B * 16; e += kConsumerThreads) {
-                const int ti = e >> 4, c = e & 15;
-                const long long head = c < 8 ? p.Hq + h : p.Hq + p.Hkv + h;
-                cp_async16(smem_u32(c < 8 ? raw_k : raw_v) + ti * 128 + (c & 7) * 16,
-                           qkv_rows + ti * row_w * 2 + head * 128 + (c & 7) * 16);
-            }
-        }
-        if (QKNORM) {
-            // RoPE angles of the B tokens: fp64 product and reduction to
-            // [-pi, pi], then an accurate fp32 sincos.
-            long long pos[2] = {0, 0};
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int e = ctid + q * kConsumerThreads;
-                if (e < p.B * 32) {
-                    const long long t = static_cast<long long>(r) * p.B + (e >> 5);
-                    pos[q] = p.pos_i64 ? reinterpret_cast<const long long *>(p.positions)[t]
-                                       : reinterpret_cast<const int *>(p.positions)[t];
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int e = ctid + q * kConsumerThreads;
-                if (e < p.B * 32) {
-                    const double theta = static_cast<double>(pos[q]) * p.inv_freq[e & 31];
-                    const double turns = rint(theta * 0.15915494309189535);
-                    double red = fma(-turns, 6.283185307179586, theta);
-                    red = fma(-turns, 2.4492935982947064e-16, red);
-                    float sn, cs;
-                    sincosf(static_cast<float>(red), &sn, &cs);
-                    trig[e] = make_float2(cs * p.rope_mscale, sn * p.rope_mscale);
-                }
-            }
-        }
-        cp_async_wait_all();
-        named_bar_sync(1, kConsumerThreads);
-
-        // ---- normalise / rotate into the swizzled operand tiles.
-        const int prep_rows = with_block ? kRows + 32 : kRows;
-        for (int pr = warp; pr < prep_rows; pr += kConsumerWarps) {
-            if (pr < kRows) {
-                if (pr < rows) {
-                    const int g = pr / p.B, ti = pr - g * p.B;
-                    const int idx = (ti * kG + g) * kD;
-                    prep_row<QKNORM>(qtile, pr, bf16_at(raw_q, idx + lane), bf16_at(raw_q, idx + lane + 32),
-                                     wq_lo, wq_hi, p.eps, QKNORM ? trig[ti * 32 + lane] : make_float2(1.f, 0.f),
-                                     lane);
-                } else {
-                    zero_row(qtile, pr, lane);
-                }
-            } else if (pr < kRows + 16) {
-                const int j = pr - kRows;
-                if (j < p.B)
-                    prep_row<QKNORM>(bk, j, bf16_at(raw_k, j * kD + lane), bf16_at(raw_k, j * kD + lane + 32),
-                                     wk_lo, wk_hi, p.eps, QKNORM ? trig[j * 32 + lane] : make_float2(1.f, 0.f),
-                                     lane);
-                else
-                    zero_row(bk, j, lane);
-            } else {
-                const int j = pr - kRows - 16;
-                if (j < p.B)
-                    prep_row<false>(bv, j, bf16_at(raw_v, j * kD + lane), bf16_at(raw_v, j * kD + lane + 32), 1.f,
-                                    1.f, 0.f, make_float2(1.f, 0.f), lane);
-                else
-                    zero_row(bv, j, lane);
-            }
-        }
-        named_bar_sync(1, kConsumerThreads);
-        uint32_t qf[4][4];
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            ldsm_x4(smem_u32(qtile) + swz(rb * 16 + (mi & 1) * 8 + rr, kk * 2 + (mi >> 1)), qf[kk][0], qf[kk][1],
-                    qf[kk][2], qf[kk][3]);
-
-        for (int jc = j0; jc < j1; ++jc) {
-            RowState st;
-            st.m[0] = st.m[1] = -INFINITY;
-            st.l[0] = st.l[1] = 0.f;
-#pragma unroll
-            for (int nd = 0; nd < 8; ++nd) st.o[nd][0] = st.o[nd][1] = st.o[nd][2] = st.o[nd][3] = 0.f;
-            const int i0 = jc * ch;
-            const int i1 = i0 + ch < items ? i0 + ch : items;
-            if (i0 == 0 && grp == 0 && active)
-                attend_tile<2>(st, qf, smem_u32(bk), smem_u32(bv), 0, p.B, p.scale_log2, lane);
-            for (int pg = (i0 == 0 ? 0 : i0 - 1); pg < i1 - 1; ++pg, ++k) {
-                const int s = static_cast<int>(k % kStages);
-                const uint32_t par = static_cast<uint32_t>((k / kStages) & 1);
-                const bool ok = mbar_wait(bar_full + 8 * s, par, abort_flag, p.status);
-                const int left = L - pg * kP - grp * 32;
-                if (active && ok && left > 0) {
-                    const uint32_t stage = smem_u32(smem + kOffStages + s * kStageBytes);
-                    attend_tile<4>(st, qf, stage, stage + kTileBytes, grp * 32, left < 32 ? left : 32,
-                                   p.scale_log2, lane);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-            }
-
-            // ---- merge the two key groups; write the chunk's partial.
-            float *mine = merge + (rb * 36) * 32 + lane;  // [row block][36 values][lane]
-            if (grp == 1 && active) {
-#pragma unroll
-                for (int nd = 0; nd < 8; ++nd)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) mine[(nd * 4 + c) * 32] = st.o[nd][c];
-                mine[32 * 32] = st.m[0];
-                mine[33 * 32] = st.m[1];
-                mine[34 * 32] = st.l[0];
-                mine[35 * 32] = st.l[1];
-            }
-            named_bar_sync(1, kConsumerThreads);
-            if (grp == 0 && active) {
-                float f0[2], f1[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float m1 = mine[(32 + e) * 32];
-                    const float mm = fmaxf(st.m[e], m1);
-                    f0[e] = exp2_approx(st.m[e] - mm);
-                    f1[e] = exp2_approx(m1 - mm);  // 0 when the other group saw no key
-                    st.m[e] = mm;
-                    st.l[e] = st.l[e] * f0[e] + mine[(34 + e) * 32] * f1[e];
-                }
-#pragma unroll
-                for (int nd = 0; nd < 8; ++nd) {
-                    st.o[nd][0] = st.o[nd][0] * f0[0] + mine[(nd * 4 + 0) * 32] * f1[0];
-                    st.o[nd][1] = st.o[nd][1] * f0[0] + mine[(nd * 4 + 1) * 32] * f1[0];
-                    st.o[nd][2] = st.o[nd][2] * f0[1] + mine[(nd * 4 + 2) * 32] * f1[1];
-                    st.o[nd][3] = st.o[nd][3] * f0[1] + mine[(nd * 4 + 3) * 32] * f1[1];
-                }
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    st.l[e] += __shfl_xor_sync(kFull, st.l[e], 1);
-                    st.l[e] += __shfl_xor_sync(kFull, st.l[e], 2);
-                }
-                const long long slot = static_cast<long long>(pl->cstart[u]) + jc;
-                const int ra = rb * 16 + (lane >> 2), rbw = ra + 8;
-                __nv_bfloat16 *ob = p.ws_o + slot * kPartialElems;
-                const int dq = 2 * (lane & 3);
-#pragma unroll
-                for (int nd = 0; nd < 8; ++nd) {
-                    if (ra < rows)
-                        *reinterpret_cast<uint32_t *>(ob + ra * kD + nd * 8 + dq) = pack_bf16(st.o[nd][0], st.o[nd][1]);
-                    if (rbw < rows)
-                        *reinterpret_cast<uint32_t *>(ob + rbw * kD + nd * 8 + dq) = pack_bf16(st.o[nd][2], st.o[nd][3]);
-                }
-                if ((lane & 3) == 0) {
-                    if (ra < rows) p.ws_ml[slot * kRows + ra] = make_float2(st.m[0], st.l[0]);
-                    if (rbw < rows) p.ws_ml[slot * kRows + rbw] = make_float2(st.m[1], st.l[1]);
-                }
-            }
-            named_bar_sync(1, kConsumerThreads);  // the merge area is free again
-        }
-    }
-    // Let the combine grid start launching; it waits for this grid to finish.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // ---------------------------------------------------- tcgen05 split pass --
 //
-// The same work plan, with the two contractions on the 5th-generation tensor
-// cores.  An item is the block or a group of kGroup pages (1 by default; 2
-// gives one N = 128 QK^T per two pages but only one CTA per SM).  Row warps
-// w own TMEM lane quarter q = w % 4 (and page w / 4 of a group): query row
+// The two contractions run on the 5th-generation tensor cores.  An item is
+// the block or one page.  Row warp w owns TMEM lane quarter q = w: query row
 // rho = 12*q + l (l < 12) is Q-tile row (and TMEM lane) 32*q + l.  Threads
 // l and l + 16 of the warp share that lane through the half-split TMEM
 // access (shape 16x32bx2): the first handles keys 0..31 of its page, the
 // second keys 32..63, so a row's softmax costs two threads half a page each
 // and one shuffle to share the row maximum.  The producer warp streams K/V
-// pages with TMA; one warp issues
-// the QK^T products and another the P.V products (a thread issues one MMA
-// at a time, ~156 cycles each at these shapes whatever N, so two issuers
-// double the tensor throughput of a CTA):
-//   S[b] (128 x 64g fp32, TMEM)  = Q (128 x 64, smem) . K_group^T
-//   O    (128 x 64 fp32, TMEM)  += P[b] (bf16, TMEM) . V_page   (per page)
+// pages with TMA; one warp issues the QK^T products and another the P.V
+// products (a thread issues one MMA at a time, ~156 cycles each at these
+// shapes whatever N, so two issuers double the tensor throughput of a CTA):
+//   S[b] (128 x 64 fp32, TMEM)  = Q (128 x 64, smem) . K_page^T
+//   O    (128 x 64 fp32, TMEM) += P[b] (bf16, TMEM) . V_page
 // with two S buffers so the next item's QK^T overlaps this item's softmax.
 // The softmax keeps a per-row exponent base m; P = 2^(s*scale*log2e - m) is
 // written as bf16 to TMEM buffer P[b] (each thread its half of the row's
@@ -859,46 +348,34 @@ __global__ void __launch_bounds__(kThreads, 2)
 // P <= 256 is exact enough in bf16 and fp32), so the common path never
 // touches O.
 namespace tc {
-#ifndef K3DA_TC_GROUP
-#define K3DA_TC_GROUP 1
-#endif
-constexpr int kGroup = K3DA_TC_GROUP;  // pages per item
-#ifndef K3DA_TC_STAGES
-#define K3DA_TC_STAGES (K3DA_TC_GROUP == 1 ? 4 : 5)
-#endif
-constexpr int kStages = K3DA_TC_STAGES;
-constexpr int kSets = kGroup;         // row-warp sets: set s takes page s of each group
-constexpr int kRowWarps = 4 * kSets;  // one warp per TMEM lane quarter and set
+constexpr int kStages = 4;
+constexpr int kRowWarps = 4;  // one warp per TMEM lane quarter
 constexpr int kRowThreads = 32 * kRowWarps;
 constexpr int kRowsPerQuarter = 12;
 constexpr int kProducerWarp = kRowWarps;
 constexpr int kQkWarp = kRowWarps + 1;  // issues the QK^T products (and owns the TMEM allocation)
 constexpr int kPvWarp = kRowWarps + 2;  // issues the P.V products
 constexpr int kThreads = 32 * (kRowWarps + 3);
-constexpr int kDimsPerSet = kD / kSets;  // O columns each set rescales and writes
-constexpr int kGroupBytes = kGroup * kStageBytes;  // K tiles of the group's pages, then their V tiles
-// Tensor memory: S[b] (64 columns per page of the group) at kSCols*b, O,
-// then P[b] (32 columns of bf16 pairs per page) at kColP + kPCols*b.
-constexpr uint32_t kSCols = 64u * kGroup;
+// Tensor memory: S[b] (64 columns) at 64*b, O at 128, then P[b] (32
+// columns of bf16 pairs) at kColP + 32*b.
+constexpr uint32_t kSCols = 64u;
 constexpr uint32_t kColO = 2u * kSCols;
 constexpr uint32_t kColP = kColO + 64u;
-constexpr uint32_t kPCols = 32u * kGroup;
-constexpr uint32_t kTmemUsed = kColP + 2u * kPCols;
-constexpr uint32_t kTmemCols = kTmemUsed <= 256u ? 256u : 512u;
-static_assert(kTmemUsed <= 512u, "tensor memory holds 512 columns");
-constexpr int kCtasPerSm = kTmemCols == 256u ? 2 : 1;
+constexpr uint32_t kPCols = 32u;
+constexpr uint32_t kTmemCols = 256u;
+static_assert(kColP + 2u * kPCols <= kTmemCols, "tensor memory columns");
+constexpr int kCtasPerSm = 2;  // 2 x 256 of the SM's 512 TMEM columns
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // Shared memory (offsets from a 1024-byte aligned base).
-constexpr int kOffStages = 0;                        // kStages x kGroupBytes
-constexpr int kOffQ = kStages * kGroupBytes;         // 128 rows x 128 B, 128B swizzle
+constexpr int kOffStages = 0;                        // kStages x (K tile, V tile)
+constexpr int kOffQ = kStages * kStageBytes;         // 128 rows x 128 B, 128B swizzle
 constexpr int kBlkRows = 16;                          // block tiles: B <= 8 keys, one 16-row MMA step
 constexpr int kOffBlkK = kOffQ + 128 * 128;          // kBlkRows rows x 128 B
 constexpr int kOffBlkV = kOffBlkK + kBlkRows * 128;  // kBlkRows rows x 128 B
 constexpr int kOffRaw = kOffBlkV + kBlkRows * 128;   // raw q [8][6][64], k [8][64], v [8][64]
 constexpr int kOffTrig = kOffRaw + kMaxB * (kG + 2) * kD * 2;  // [8][32] float2
 constexpr int kOffNormW = kOffTrig + kMaxB * 32 * 8;  // q and k norm weights, [2][64] bf16
-constexpr int kOffXch = kOffNormW + 2 * kD * 2;      // row max [2][kSets][128], row sum [kSets][128]
-constexpr int kOffPlan = kOffXch + (kSets > 1 ? 3 * kSets * 128 * 4 : 0);  // one set exchanges nothing
+constexpr int kOffPlan = kOffNormW + 2 * kD * 2;
 constexpr int kNumBars = 2 * kStages + 8;  // full, empty, s_full[2], p_full[2], o_done[2], q_ready, done
 constexpr int kOffBar = kOffPlan + (static_cast<int>(sizeof(Plan)) + 15) / 16 * 16;
 constexpr int kOffTaddr = kOffBar + kNumBars * 8;
@@ -907,7 +384,7 @@ constexpr int kSmemUsed = kOffFlag + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 // Two CTAs per SM: 228 KB per SM, 1 KB of it reserved per CTA.
-static_assert(kCtasPerSm == 1 || 2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs fit an SM's shared memory");
+static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs fit an SM's shared memory");
 static_assert(kOffQ % 1024 == 0 && kOffBlkK % 1024 == 0 && kOffBlkV % 1024 == 0, "SW128 tiles need 1 KB alignment");
 static_assert(kOffBar % 8 == 0 && kOffPlan % 8 == 0, "mbarrier / int64 alignment");
 
@@ -917,7 +394,7 @@ static_assert(kOffBar % 8 == 0 && kOffPlan % 8 == 0, "mbarrier / int64 alignment
 constexpr uint32_t idesc_f16(uint32_t m, uint32_t n, bool b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? 1u << 16 : 0u) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
-constexpr uint32_t kIdescQK = idesc_f16(128, 64 * kGroup, false);  // a page group's keys
+constexpr uint32_t kIdescQK = idesc_f16(128, 64, false);            // a page's keys
 constexpr uint32_t kIdescQKBlock = idesc_f16(128, kBlkRows, false); // the block tile
 constexpr uint32_t kIdescPV = idesc_f16(128, 64, true);
 
@@ -977,13 +454,6 @@ __device__ __forceinline__ void tmem_ld_h32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_ld_h16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16], 16;"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-                 : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 __device__ __forceinline__ void tmem_st_h32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile("tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%0], 32, {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
                  : "memory");
@@ -999,52 +469,7 @@ __device__ __forceinline__ void tmem_st_h16(uint32_t taddr, const uint32_t (&r)[
 template <bool QKNORM>
 __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     k3da_tc_kernel(const __grid_constant__ CUtensorMap pool_map, const __grid_constant__ Params p) {
-    constexpr auto kStages = tc::kStages;
-    constexpr auto kGroup = tc::kGroup;
-    constexpr auto kGroupBytes = tc::kGroupBytes;
-    constexpr auto kSCols = tc::kSCols;
-    constexpr auto kPCols = tc::kPCols;
-    constexpr auto kIdescQKBlock = tc::kIdescQKBlock;
-    constexpr auto kRowWarps = tc::kRowWarps;
-    constexpr auto kRowThreads = tc::kRowThreads;
-    constexpr auto kRowsPerQuarter = tc::kRowsPerQuarter;
-    constexpr auto kProducerWarp = tc::kProducerWarp;
-    constexpr auto kQkWarp = tc::kQkWarp;
-    constexpr auto kPvWarp = tc::kPvWarp;
-    constexpr auto kThreads = tc::kThreads;
-    constexpr auto kTmemCols = tc::kTmemCols;
-    constexpr auto kColO = tc::kColO;
-    constexpr auto kColP = tc::kColP;
-    constexpr auto kRescaleThreshold = tc::kRescaleThreshold;
-    constexpr auto kOffStages = tc::kOffStages;
-    constexpr auto kOffQ = tc::kOffQ;
-    constexpr auto kOffBlkK = tc::kOffBlkK;
-    constexpr auto kOffBlkV = tc::kOffBlkV;
-    constexpr auto kBlkRows = tc::kBlkRows;
-    constexpr auto kOffRaw = tc::kOffRaw;
-    constexpr auto kOffTrig = tc::kOffTrig;
-    constexpr auto kOffNormW = tc::kOffNormW;
-    constexpr auto kOffXch = tc::kOffXch;
-    constexpr auto kSets = tc::kSets;
-    constexpr auto kDimsPerSet = tc::kDimsPerSet;
-    constexpr auto kOffPlan = tc::kOffPlan;
-    constexpr auto kOffBar = tc::kOffBar;
-    constexpr auto kOffTaddr = tc::kOffTaddr;
-    constexpr auto kOffFlag = tc::kOffFlag;
-    constexpr auto kIdescQK = tc::kIdescQK;
-    constexpr auto kIdescPV = tc::kIdescPV;
-    using tc::desc_sw128;
-    using tc::mma_ss;
-    using tc::mma_ts;
-    using tc::mma_commit;
-    using tc::fence_before;
-    using tc::fence_after;
-    using tc::tmem_st32;
-    using tc::tmem_wait_st;
-    using tc::tmem_ld_h32;
-    using tc::tmem_ld_h16;
-    using tc::tmem_st_h32;
-    using tc::tmem_st_h16;
+    using namespace tc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1057,7 +482,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     const uint32_t bar_odone = bar_pfull + 16, bar_qready = bar_odone + 16, bar_done = bar_qready + 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    build_plan<tc::kGroup>(p, pl, blockIdx.x, p.grid, blockIdx.x == 0);
+    build_plan(p, pl, blockIdx.x, p.grid, blockIdx.x == 0);
     {
         // Q and block tiles start as zeros: rows without a query row or a
         // block token stay zero for the whole kernel.
@@ -1104,7 +529,6 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         // The CTA's pages, run after run, form one sequence; lane l resolves
         // entry base + l of each 32-entry batch (page id -> TMA row of its K
         // tile, -1 if out of range), one batch ahead of the loads it feeds.
-        // Each stage takes one item: up to kGroup pages of one run.
         uint64_t policy;
         asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
         const int total = pl->run_pq[nrun];
@@ -1119,73 +543,42 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
             if (page < 0 || page >= p.num_pages) return -1;  // served as zeros, flagged
             return ((page * 2 + 0) * p.Hkv + h) * kP;
         };
-        int base = 0, cur = resolve(lane), nxt = resolve(32 + lane);
-        int q = 0;
-        long long k = 0;  // items loaded
-        for (int rn = 0; rn < nrun; ++rn) {
-            const int npg = pl->run_pq[rn + 1] - pl->run_pq[rn];
-            for (int g0 = 0; g0 < npg; g0 += kGroup, ++k) {
-                const int cnt = npg - g0 < kGroup ? npg - g0 : kGroup;
-                int krow[kGroup];
-#pragma unroll
-                for (int j = 0; j < kGroup; ++j) {
-                    krow[j] = -2;  // no page
-                    if (j < cnt) {
-                        if (q >= base + 32) {
-                            base += 32;
-                            cur = nxt;
-                            nxt = resolve(base + 32 + lane);
-                        }
-                        krow[j] = __shfl_sync(kFull, cur, q - base);
-                        ++q;
-                    }
-                }
-                const int s = static_cast<int>(k % kStages);
-                const uint32_t par = static_cast<uint32_t>((k / kStages) & 1);
-                mbar_wait(bar_empty + 8 * s, par ^ 1u, abort_flag, p.status);
-                uint8_t *stage = smem + kOffStages + s * kGroupBytes;
-                int bytes = 0;
-#pragma unroll
-                for (int j = 0; j < kGroup; ++j) {
-                    if (krow[j] >= 0) {
-                        bytes += kStageBytes;
-                    } else if (krow[j] == -1) {
-                        // Out-of-range page id: flag it and serve zeros.
-                        if (lane == 0 && p.status) atomicOr(p.status, K3DA_STATUS_BAD_PAGE);
-                        uint4 *dk = reinterpret_cast<uint4 *>(stage + j * kTileBytes);
-                        uint4 *dv = reinterpret_cast<uint4 *>(stage + (kGroup + j) * kTileBytes);
-                        for (int e = lane; e < kTileBytes / 16; e += 32) {
-                            dk[e] = make_uint4(0, 0, 0, 0);
-                            dv[e] = make_uint4(0, 0, 0, 0);
-                        }
-                    }
-                }
-                if (bytes < cnt * kStageBytes) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) {
-                    if (bytes > 0) {
-                        mbar_arrive_expect_tx(bar_full + 8 * s, bytes);
-#pragma unroll
-                        for (int j = 0; j < kGroup; ++j) {
-                            if (krow[j] >= 0) {
-                                tma_load_tile(smem_u32(stage + j * kTileBytes), &pool_map, krow[j], bar_full + 8 * s,
-                                              policy);
-                                tma_load_tile(smem_u32(stage + (kGroup + j) * kTileBytes), &pool_map,
-                                              krow[j] + p.Hkv * kP, bar_full + 8 * s, policy);
-                            }
-                        }
-                    } else {
-                        mbar_arrive(bar_full + 8 * s);
-                    }
-                }
-                __syncwarp();
+        int cur = resolve(lane), nxt = resolve(32 + lane);
+        for (int q = 0; q < total; ++q) {
+            if (q > 0 && (q & 31) == 0) {
+                cur = nxt;
+                nxt = resolve(q + 32 + lane);
             }
+            const int krow = __shfl_sync(kFull, cur, q & 31);
+            const int s = q % kStages;
+            const uint32_t par = static_cast<uint32_t>((q / kStages) & 1);
+            mbar_wait(bar_empty + 8 * s, par ^ 1u, abort_flag, p.status);
+            uint8_t *stage = smem + kOffStages + s * kStageBytes;
+            if (krow < 0) {
+                // Out-of-range page id: flag it and serve zeros.
+                if (lane == 0 && p.status) atomicOr(p.status, K3DA_STATUS_BAD_PAGE);
+                uint4 *dz = reinterpret_cast<uint4 *>(stage);
+                for (int e = lane; e < kStageBytes / 16; e += 32) dz[e] = make_uint4(0, 0, 0, 0);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            __syncwarp();
+            if (lane == 0) {
+                if (krow >= 0) {
+                    mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
+                    tma_load_tile(smem_u32(stage), &pool_map, krow, bar_full + 8 * s, policy);
+                    tma_load_tile(smem_u32(stage + kTileBytes), &pool_map, krow + p.Hkv * kP, bar_full + 8 * s,
+                                  policy);
+                } else {
+                    mbar_arrive(bar_full + 8 * s);
+                }
+            }
+            __syncwarp();
         }
         // Drain: every issued load must land before the CTA exits (matters
         // only when a wait gave up and the consumers stopped early).
         if (*abort_flag) {
-            for (long long j = (k > kStages ? k - kStages : 0); j < k; ++j) {
-                const int s = static_cast<int>(j % kStages);
+            for (int j = (total > kStages ? total - kStages : 0); j < total; ++j) {
+                const int s = j % kStages;
                 const uint32_t par = static_cast<uint32_t>((j / kStages) & 1);
                 const unsigned long long t0 = global_ns();
                 while (!mbar_try_wait(bar_full + 8 * s, par) && global_ns() - t0 < kWaitLimitNs) {
@@ -1197,11 +590,9 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         // A thread issues one tcgen05.mma at a time (about 156 cycles each at
         // these shapes, whatever N), so the two products have an issuing
         // warp each.  The QK^T warp fills S[b] for item i once the row warps
-        // have released it (item i-2 done); a page group's K tiles sit back
-        // to back, so its QK^T is one N = 64*kGroup product.  The P.V warp
-        // accumulates O once item i's P is in TMEM, one product per page
-        // present, then releases the stage (QK^T of the item completed
-        // before its softmax began).
+        // have released it (item i-2 done).  The P.V warp accumulates O once
+        // item i's P is in TMEM, then releases the page's stage (the item's
+        // QK^T completed before its softmax began).
         const bool is_qk = warp == kQkWarp;
         const uint64_t q_desc = desc_sw128(smem_u32(smem + kOffQ));
         const uint64_t bk_desc = desc_sw128(smem_u32(smem + kOffBlkK));
@@ -1209,8 +600,6 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         long long it = 0, kr = 0;
         for (int rn = 0; rn < nrun; ++rn) {
             const int u = pl->run_u[rn];
-            const int r = u / p.Hkv;
-            const int npages = (pl->lens[r] + kP - 1) / kP;
             const int ch = pl->ch[u];
             const int items = static_cast<int>(pl->ustart[u + 1] - pl->ustart[u]);
             if (is_qk) {
@@ -1223,11 +612,6 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                 for (int item = i0; item < i1; ++item, ++it) {
                     const int b = static_cast<int>(it & 1);
                     const bool is_page = item > 0;
-                    int cnt = 0;
-                    if (is_page) {
-                        const int left = npages - (item - 1) * kGroup;
-                        cnt = left < kGroup ? left : kGroup;
-                    }
                     const int s = static_cast<int>(kr % kStages);
                     if (is_page) ++kr;
                     if (is_qk) {
@@ -1243,7 +627,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                         }
                         if (lane == 0) {
                             const uint64_t k_desc =
-                                is_page ? desc_sw128(smem_u32(smem + kOffStages + s * kGroupBytes)) : bk_desc;
+                                is_page ? desc_sw128(smem_u32(smem + kOffStages + s * kStageBytes)) : bk_desc;
                             const uint32_t idesc = is_page ? kIdescQK : kIdescQKBlock;
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
@@ -1258,22 +642,19 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                         fence_after();
                         if (lane == 0) {
                             const uint32_t pcol = tmem + kColP + kPCols * b;
-                            if (cnt == 0) {
+                            if (!is_page) {
                                 // The block: at most 8 keys, all in the first 16-key step.
                                 mma_ts(tmem + kColO, pcol, bv_desc, kIdescPV, first ? 0u : 1u);
                             } else {
-                                const uint32_t vbase =
-                                    smem_u32(smem + kOffStages + s * kGroupBytes + kGroup * kTileBytes);
-                                for (int pg = 0; pg < cnt; ++pg) {
-                                    const uint64_t v_desc = desc_sw128(vbase + pg * kTileBytes);
+                                const uint64_t v_desc =
+                                    desc_sw128(smem_u32(smem + kOffStages + s * kStageBytes + kTileBytes));
 #pragma unroll
-                                    for (int kk = 0; kk < 4; ++kk)
-                                        mma_ts(tmem + kColO, pcol + 32u * pg + 8u * kk, v_desc + ((kk * 2048) >> 4),
-                                               kIdescPV, (pg > 0 || kk > 0 || !first) ? 1u : 0u);
-                                }
+                                for (int kk = 0; kk < 4; ++kk)
+                                    mma_ts(tmem + kColO, pcol + 8u * kk, v_desc + ((kk * 2048) >> 4), kIdescPV,
+                                           (kk > 0 || !first) ? 1u : 0u);
                             }
                             mma_commit(bar_odone + 8 * b);  // o_done[it & 1]
-                            if (cnt > 0) mma_commit(bar_empty + 8 * s);
+                            if (is_page) mma_commit(bar_empty + 8 * s);
                         }
                         __syncwarp();
                     }
@@ -1287,20 +668,14 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         }
     } else if (warp < kRowWarps && nrun > 0) {
         // ------------------------------------------- softmax / row warps --
-        // Warp w serves TMEM lane quarter w % 4 and, within each page
-        // group, page w / 4 (its set).  The sets of a row share one
-        // exponent base: they swap their row maxima through shared memory
-        // at every item, and add their row sums at a chunk's end.
         const int t = threadIdx.x;
-        const int q = warp & 3;
-        const int set = warp >> 2;
+        const int q = warp;
         const int half = lane >> 4;               // key half of this thread
         const int l16 = lane & 15;
         const int rho = l16 < kRowsPerQuarter ? q * kRowsPerQuarter + l16 : 1 << 20;
         const int rows = kG * p.B;
         const bool active = rho < rows;
         const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
-        const int tl = 32 * q + lane;             // exchange slot of this thread (row, key half)
         uint8_t *qtile = smem + kOffQ;
         uint8_t *bk = smem + kOffBlkK;
         uint8_t *bv = smem + kOffBlkV;
@@ -1308,12 +683,10 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         uint8_t *raw_k = raw_q + kMaxB * kG * kD * 2;
         uint8_t *raw_v = raw_k + kMaxB * kD * 2;
         float2 *trig = reinterpret_cast<float2 *>(smem + kOffTrig);
-        float *xmax = reinterpret_cast<float *>(smem + kOffXch);  // [2][kSets][128]
-        float *xsum = xmax + 2 * kSets * 128;                      // [kSets][128]
         const long long row_w = static_cast<long long>(p.Hq + 2 * p.Hkv) * kD;
         __nv_bfloat16 *normw = reinterpret_cast<__nv_bfloat16 *>(smem + kOffNormW);  // [0..63] q, [64..127] k
         if (QKNORM && t < 2 * kD) normw[t] = t < kD ? p.q_w[t] : p.k_w[t - kD];
-        if (set == 0) {
+        {
             // Rows sit in TMEM lanes 0-11 of each quarter and P is written
             // below for lanes 0-15 only: zero the P columns of the whole
             // quarter once so the P.V products of the unused lanes read zeros.
@@ -1323,6 +696,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
 #pragma unroll
             for (uint32_t c = 0; c < 2u * kPCols; c += 32u) tmem_st32(tmem + lane_off + kColP + c, zero);
             tmem_wait_st();
+            fence_before();
         }
         // A chunk's partial is written while the next chunk's first item is in
         // flight (its P.V, the last O reader, was confirmed just before), so
@@ -1331,38 +705,23 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         long long epi_slot = 0;
         float epi_m = 0.f, epi_l = 0.f;
         auto write_partial = [&]() {
-            // Set s writes O columns [kDimsPerSet*s, +kDimsPerSet) of the
-            // row's one TMEM lane: thread half 0 the first half of them, half
-            // 1 the second.  The row sum adds the two halves' key shares.
-            float ltot = epi_l + __shfl_xor_sync(kFull, epi_l, 16);
-            if (kSets > 1) {
-                xsum[set * 128 + tl] = ltot;
-                named_bar_sync(2, kRowThreads);
-                ltot = 0.f;
-#pragma unroll
-                for (int s2 = 0; s2 < kSets; ++s2) ltot += xsum[s2 * 128 + tl];
-            }
-            constexpr int kKeep = kDimsPerSet / 2;
-            uint32_t orr[kKeep];
-            if constexpr (kKeep == 32)
-                tmem_ld_h32(tmem + lane_off + kColO + kDimsPerSet * set, *reinterpret_cast<uint32_t(*)[32]>(orr));
-            else
-                tmem_ld_h16(tmem + lane_off + kColO + kDimsPerSet * set, *reinterpret_cast<uint32_t(*)[16]>(orr));
-            float outv[kKeep];
-#pragma unroll
-            for (int j = 0; j < kKeep; ++j) outv[j] = __uint_as_float(orr[j]);
+            // Thread half 0 writes O columns 0-31 of the row's TMEM lane,
+            // half 1 columns 32-63.  The row sum adds the two halves' shares.
+            const float ltot = epi_l + __shfl_xor_sync(kFull, epi_l, 16);
+            uint32_t orr[32];
+            tmem_ld_h32(tmem + lane_off + kColO, orr);
             if (active) {
                 // The partial's O leaves as bf16: half the bytes for the
                 // split pass to write and the combine to read; one rounding
                 // (2^-9 relative) of values the combine then averages.
-                uint4 *dst = reinterpret_cast<uint4 *>(p.ws_o + epi_slot * kPartialElems + rho * kD +
-                                                       kDimsPerSet * set + kKeep * half);
+                uint4 *dst = reinterpret_cast<uint4 *>(p.ws_o + epi_slot * kPartialElems + rho * kD + 32 * half);
 #pragma unroll
-                for (int j = 0; j < kKeep / 8; ++j)
-                    dst[j] = make_uint4(pack_bf16(outv[8 * j], outv[8 * j + 1]), pack_bf16(outv[8 * j + 2], outv[8 * j + 3]),
-                                        pack_bf16(outv[8 * j + 4], outv[8 * j + 5]),
-                                        pack_bf16(outv[8 * j + 6], outv[8 * j + 7]));
-                if (half == 0 && set == 0) p.ws_ml[epi_slot * kRows + rho] = make_float2(epi_m, ltot);
+                for (int j = 0; j < 4; ++j)
+                    dst[j] = make_uint4(pack_bf16(__uint_as_float(orr[8 * j]), __uint_as_float(orr[8 * j + 1])),
+                                        pack_bf16(__uint_as_float(orr[8 * j + 2]), __uint_as_float(orr[8 * j + 3])),
+                                        pack_bf16(__uint_as_float(orr[8 * j + 4]), __uint_as_float(orr[8 * j + 5])),
+                                        pack_bf16(__uint_as_float(orr[8 * j + 6]), __uint_as_float(orr[8 * j + 7])));
+                if (half == 0) p.ws_ml[epi_slot * kRows + rho] = make_float2(epi_m, ltot);
             }
             epi_pending = false;
         };
@@ -1524,24 +883,23 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                     const int b = static_cast<int>(it & 1);
                     const bool is_page = item > 0;
                     const int s = static_cast<int>(kr % kStages);
-                    constexpr int kKeys = kP * kGroup;  // keys of a page group
                     int valid = p.B;
                     if (is_page) {
-                        const int left = L - (item - 1) * kKeys;
-                        valid = left < kKeys ? left : kKeys;
+                        const int left = L - (item - 1) * kP;
+                        valid = left < kP ? left : kP;
                     }
                     mbar_wait(bar_sfull + 8 * b, static_cast<uint32_t>((it >> 1) & 1), abort_flag, p.status);
                     fence_after();
-                    // This thread's half of the keys of page `set` of the group.
+                    // This thread's half of the page's keys.
                     float sv[32];
                     {
                         uint32_t sr[32];
-                        tmem_ld_h32(tmem + lane_off + kSCols * b + 64u * set, sr);
+                        tmem_ld_h32(tmem + lane_off + kSCols * b, sr);
 #pragma unroll
                         for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(sr[j]);
                     }
-                    if (valid < kKeys) {
-                        const int lim = valid - 64 * set - 32 * half;
+                    if (valid < kP) {
+                        const int lim = valid - 32 * half;
 #pragma unroll
                         for (int j = 0; j < 32; ++j) sv[j] = j < lim ? sv[j] : -INFINITY;
                     }
@@ -1552,15 +910,6 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                     for (int j = 4; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], sv[j]);
                     float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                     rmax = fmaxf(rmax, __shfl_xor_sync(kFull, rmax, 16)) * p.scale_log2;
-                    if (kSets > 1) {
-                        // Row max over the sets (key 0 of page 0 is always
-                        // valid, so the result is finite).
-                        float *xm = xmax + (it & 1) * kSets * 128;
-                        xm[set * 128 + tl] = rmax;
-                        named_bar_sync(2, kRowThreads);
-#pragma unroll
-                        for (int s2 = 0; s2 < kSets; ++s2) rmax = fmaxf(rmax, xm[s2 * 128 + tl]);
-                    }
                     // Exponent base: the row max on a chunk's first item; later,
                     // only when the max passes the base by more than 2^8.
                     const bool first = item == i0;
@@ -1577,9 +926,9 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                             rs[j & 3] += p0 + p1;
                             pk[j] = pack_bf16(p0, p1);
                         }
-                        // The row's P for page `set`: this thread's half of
-                        // the keys, 16 columns of bf16 pairs.
-                        tmem_st_h16(tmem + lane_off + kColP + kPCols * b + 32u * set, pk);
+                        // The row's P: this thread's half of the keys, 16
+                        // columns of bf16 pairs.
+                        tmem_st_h16(tmem + lane_off + kColP + kPCols * b, pk);
                     }
                     lsum = (first ? 0.f : lsum * f) + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
                     m_used = m_new;
@@ -1599,31 +948,21 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                     }
                     if (epi_pending) write_partial();  // before this item's P.V overwrites O
                     if (__any_sync(kFull, need)) {
-                        // Each set rescales its own O columns of the row,
-                        // the two thread halves one half of them each.
-                        const uint32_t col = tmem + lane_off + kColO + kDimsPerSet * set;
-                        constexpr int kHalf = kDimsPerSet / 2;
-                        uint32_t part[kHalf];
-                        if constexpr (kHalf == 32)
-                            tmem_ld_h32(col, *reinterpret_cast<uint32_t(*)[32]>(part));
-                        else
-                            tmem_ld_h16(col, *reinterpret_cast<uint32_t(*)[16]>(part));
+                        // The row's two threads rescale one half of its O each.
+                        const uint32_t col = tmem + lane_off + kColO;
+                        uint32_t part[32];
+                        tmem_ld_h32(col, part);
 #pragma unroll
-                        for (int j = 0; j < kHalf; ++j) part[j] = __float_as_uint(__uint_as_float(part[j]) * f);
-                        if constexpr (kHalf == 32)
-                            tmem_st_h32(col, *reinterpret_cast<uint32_t(*)[32]>(part));
-                        else
-                            tmem_st_h16(col, *reinterpret_cast<uint32_t(*)[16]>(part));
+                        for (int j = 0; j < 32; ++j) part[j] = __float_as_uint(__uint_as_float(part[j]) * f);
+                        tmem_st_h32(col, part);
                         tmem_wait_st();
                     }
-                    if (is_page && (valid & (kP - 1)) != 0) {
+                    if (is_page && valid < kP) {
                         // Stale pool slots past the context may hold
-                        // non-finite values: zero them in the group's last
-                        // page before P.V reads them.
-                        const int lp = valid / kP, lv = valid - lp * kP;
-                        uint4 *vt = reinterpret_cast<uint4 *>(smem + kOffStages + s * kGroupBytes +
-                                                              (kGroup + lp) * kTileBytes);
-                        for (int e = t; e < (kP - lv) * 8; e += kRowThreads) vt[lv * 8 + e] = make_uint4(0, 0, 0, 0);
+                        // non-finite values: zero them in the page's V tile
+                        // before P.V reads them.
+                        uint4 *vt = reinterpret_cast<uint4 *>(smem + kOffStages + s * kStageBytes + kTileBytes);
+                        for (int e = t; e < (kP - valid) * 8; e += kRowThreads) vt[valid * 8 + e] = make_uint4(0, 0, 0, 0);
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     }
                     fence_before();
@@ -1776,24 +1115,10 @@ __global__ void __launch_bounds__(128) k3da_wait_selftest_kernel(int32_t *status
     __syncthreads();
 }
 
-// The split pass that runs: the tcgen05 one unless built with
-// K3DA_USE_TCGEN05=0 (the mma.sync one).
-#ifndef K3DA_USE_TCGEN05
-#define K3DA_USE_TCGEN05 1
-#endif
-#if K3DA_USE_TCGEN05
 constexpr int kSplitThreads = tc::kThreads;
 constexpr int kSplitSmem = tc::kSmemBytes;
-constexpr int kSplitGroup = tc::kGroup;
-#define kSplitLaunch k3da_tc_kernel
-#else
-constexpr int kSplitThreads = kThreads;
-constexpr int kSplitSmem = kSmemBytes;
-constexpr int kSplitGroup = 1;
-#define kSplitLaunch k3da_split_kernel
-#endif
-const void *const kSplitKernel[2] = {reinterpret_cast<const void *>(&kSplitLaunch<false>),
-                                     reinterpret_cast<const void *>(&kSplitLaunch<true>)};
+const void *const kSplitKernel[2] = {reinterpret_cast<const void *>(&k3da_tc_kernel<false>),
+                                     reinterpret_cast<const void *>(&k3da_tc_kernel<true>)};
 
 // CTAs of `kernel` that fit on one SM: registers (per-warp allocation in
 // units of 256), shared memory (with the per-block reservation), threads,
@@ -1817,15 +1142,14 @@ int occupancy_of(const void *kernel, int threads, int dyn_smem, int dev, int *oc
     const int smem_block = static_cast<int>(fa.sharedSizeBytes) + dyn_smem + smem_rsv;
     n = n < smem_sm / smem_block ? n : smem_sm / smem_block;
     n = n < thr_sm / (warps * 32) ? n : thr_sm / (warps * 32);
-#if K3DA_USE_TCGEN05
     n = n < static_cast<int>(512 / tc::kTmemCols) ? n : static_cast<int>(512 / tc::kTmemCols);
-#endif
     *occ = n;
     return K3DA_OK;
 }
 
 struct DeviceConfig {
     bool ready;
+    unsigned long long ctx_id;  // context the kernels were configured in
     int sms;
     int occupancy[2];  // CTAs per SM of the split kernel: [plain, qknorm]
 };
@@ -1834,52 +1158,80 @@ std::mutex g_mutex;
 thread_local cudaEvent_t g_phase_event = nullptr;
 DeviceConfig g_devices[128];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
 
+template <typename Fn>
+bool driver_entry(const char *name, int version, Fn *out) {
+    if (*out != nullptr) return true;
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion(name, &fn, version, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return false;
+    *out = reinterpret_cast<Fn>(fn);
+    return true;
+}
+
+// Process-unique id of the context current on this thread (the device's
+// primary context once the runtime has used it).  A device reset makes a new
+// context with a new id, so state tied to the old one is set up again.
+// Called with g_mutex held.
+int current_context_id(int dev, unsigned long long *id) {
+    if (!driver_entry("cuCtxGetCurrent", 4000, &g_ctx_current) || !driver_entry("cuCtxGetId", 12000, &g_ctx_id))
+        return K3DA_ECUDA;
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) {
+        // No context on this thread yet: cudaSetDevice binds the device's
+        // primary context.
+        if (cudaSetDevice(dev) != cudaSuccess) return K3DA_ECUDA;
+        if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return K3DA_ECUDA;
+    }
+    return g_ctx_id(ctx, id) == CUDA_SUCCESS ? K3DA_OK : K3DA_ECUDA;
+}
+
+// Configures the split kernel on `dev` (shared-memory attributes, grid size)
+// once per context of that device; later calls return the stored values.
 int configure_device(int dev, DeviceConfig *cfg) {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (dev < 0 || dev >= 128) return K3DA_EINVAL;
     DeviceConfig &d = g_devices[dev];
-    if (!d.ready) {
-        int prev = -1;
-        if (cudaGetDevice(&prev) != cudaSuccess) return K3DA_ECUDA;
-        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) return K3DA_ECUDA;
-        int rc = K3DA_OK;
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess) return K3DA_ECUDA;
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) return K3DA_ECUDA;
+    unsigned long long ctx = 0;
+    int rc = current_context_id(dev, &ctx);
+    if (rc == K3DA_OK && (!d.ready || d.ctx_id != ctx)) {
+        d.ready = false;
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) rc = K3DA_ECUDA;
-        const void *kernels[2] = {kSplitKernel[0], kSplitKernel[1]};
         int occ[2] = {0, 0};
         for (int v = 0; v < 2 && rc == K3DA_OK; ++v) {
             // Ask for the largest shared-memory carveout, then size the grid
             // from the occupancy it allows.
-            if (cudaFuncSetAttribute(kernels[v], cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem) !=
+            if (cudaFuncSetAttribute(kSplitKernel[v], cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem) !=
                     cudaSuccess ||
-                cudaFuncSetAttribute(kernels[v], cudaFuncAttributePreferredSharedMemoryCarveout,
+                cudaFuncSetAttribute(kSplitKernel[v], cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared) != cudaSuccess)
                 rc = K3DA_ECUDA;
             else
-                rc = occupancy_of(kernels[v], kSplitThreads, kSplitSmem, dev, &occ[v]);
+                rc = occupancy_of(kSplitKernel[v], kSplitThreads, kSplitSmem, dev, &occ[v]);
         }
-        if (rc == K3DA_OK && g_encode == nullptr) {
-            cudaDriverEntryPointQueryResult q;
-            void *fn = nullptr;
-            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                    cudaSuccess ||
-                q != cudaDriverEntryPointSuccess || fn == nullptr)
-                rc = K3DA_ECUDA;
-            else
-                g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-        }
-        if (prev != dev) cudaSetDevice(prev);
-        if (rc != K3DA_OK) return rc;
-        for (int v = 0; v < 2; ++v) {
-            if (occ[v] < 1) return K3DA_ECUDA;
+        if (rc == K3DA_OK && !driver_entry("cuTensorMapEncodeTiled", 12000, &g_encode)) rc = K3DA_ECUDA;
+        for (int v = 0; v < 2 && rc == K3DA_OK; ++v) {
+            if (occ[v] < 1) rc = K3DA_ECUDA;
             if (occ[v] > kMaxCtasPerSm) occ[v] = kMaxCtasPerSm;
         }
-        d.sms = sms;
-        d.occupancy[0] = occ[0];
-        d.occupancy[1] = occ[1];
-        d.ready = true;
+        if (rc == K3DA_OK) {
+            d.sms = sms;
+            d.occupancy[0] = occ[0];
+            d.occupancy[1] = occ[1];
+            d.ctx_id = ctx;
+            d.ready = true;
+        }
     }
+    if (prev != dev) cudaSetDevice(prev);
+    if (rc != K3DA_OK) return rc;
     *cfg = d;
     return K3DA_OK;
 }
@@ -1887,21 +1239,20 @@ int configure_device(int dev, DeviceConfig *cfg) {
 bool supported_heads(int hq, int hkv) { return (hq == 6 && hkv == 1) || (hq == 24 && hkv == 4); }
 
 // Chunks a unit can have: at most chunk_splits(R*Hkv), or ceil(items/ch_max)
-// once chunks reach ch_max = kChunkMax / G items; items <= 1 + ceil(page_stride / G).
-size_t workspace_slots(int R, int Hkv, int page_stride) {
-    constexpr long long ch_max = kChunkMax / kSplitGroup > 0 ? kChunkMax / kSplitGroup : 1;
-    const long long items = 1 + (static_cast<long long>(page_stride) + kSplitGroup - 1) / kSplitGroup;
-    const long long by_len = (items + ch_max - 1) / ch_max;
+// once chunks reach ch_max = kChunkMax items; items <= 1 + page_stride.
+constexpr size_t workspace_slots(int R, int Hkv, int page_stride) {
+    const long long items = 1 + static_cast<long long>(page_stride);
+    const long long by_len = (items + kChunkMax - 1) / kChunkMax;
     const long long splits = chunk_splits(R * Hkv);
     const long long per_unit = by_len > splits ? by_len : splits;
     return static_cast<size_t>(R) * Hkv * static_cast<size_t>(per_unit);
 }
 
 constexpr size_t kWsHeaderBytes = 512;  // unit table, then the partials (16-byte aligned)
+constexpr size_t kSlotBytes = kPartialElems * 2 + kRows * 8;  // bf16 O, then (m, l) fp32 per row
 
-size_t workspace_for(int R, int Hkv, int page_stride) {
-    return kWsHeaderBytes +
-           workspace_slots(R, Hkv, page_stride) * (kPartialElems * sizeof(__nv_bfloat16) + kRows * sizeof(float2));
+constexpr size_t workspace_for(int R, int Hkv, int page_stride) {
+    return kWsHeaderBytes + workspace_slots(R, Hkv, page_stride) * kSlotBytes;
 }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -1910,24 +1261,37 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // exists on every GPU this library is loaded on, for callers that cannot
 // allocate.  8 MiB covers every shape with page_stride <= 1279.
 constexpr size_t kStaticScratchBytes = size_t(8) << 20;
+constexpr int kStaticMaxStride = 1279;
+static_assert(workspace_for(kMaxR, 4, kStaticMaxStride) <= kStaticScratchBytes &&
+                  workspace_for(kMaxR, 1, kStaticMaxStride) <= kStaticScratchBytes,
+              "the no-allocation scratch serves every page_stride up to its stated bound");
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-// Device address of g_static_scratch on `dev`, looked up once per device with
-// that device current (the host-side symbol is only a stand-in).
+// Device address of g_static_scratch on `dev` (the host-side symbol is only
+// a stand-in), looked up with that device current once per context of the
+// device: a device reset gives the device a new context, and the address is
+// looked up again in it.
 int static_scratch_address(int dev, void **out) {
     static void *addr[128] = {nullptr};
+    static unsigned long long ctx_of[128] = {0};
     std::lock_guard<std::mutex> lock(g_mutex);
     if (dev < 0 || dev >= 128) return K3DA_EINVAL;
-    if (addr[dev] == nullptr) {
-        int prev = -1;
-        if (cudaGetDevice(&prev) != cudaSuccess) return K3DA_ECUDA;
-        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) return K3DA_ECUDA;
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess) return K3DA_ECUDA;
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) return K3DA_ECUDA;
+    unsigned long long ctx = 0;
+    int rc = current_context_id(dev, &ctx);
+    if (rc == K3DA_OK && (addr[dev] == nullptr || ctx_of[dev] != ctx)) {
         void *ptr = nullptr;
-        const cudaError_t rc = cudaGetSymbolAddress(&ptr, g_static_scratch);
-        if (prev != dev) cudaSetDevice(prev);
-        if (rc != cudaSuccess || ptr == nullptr) return K3DA_ECUDA;
-        addr[dev] = ptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) {
+            rc = K3DA_ECUDA;
+        } else {
+            addr[dev] = ptr;
+            ctx_of[dev] = ctx;
+        }
     }
+    if (prev != dev) cudaSetDevice(prev);
+    if (rc != K3DA_OK) return rc;
     *out = addr[dev];
     return K3DA_OK;
 }
@@ -1943,9 +1307,9 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
         !aligned(ctx_lens, 4) || (status && !aligned(status, 4)))
         return K3DA_EINVAL;
     if (R < 1 || R > kMaxR || B < 1 || B > kMaxB || page_stride < 1 || num_pages < 1) return K3DA_EINVAL;
+    if (page_stride > kMaxPageStride) return K3DA_EINVAL;
     if (head_dim != kD || !supported_heads(Hq, Hkv)) return K3DA_EUNSUPPORTED;
     if (num_pages > ((1LL << 31) - 1) / (2LL * Hkv * kP)) return K3DA_EINVAL;
-    if (static_cast<long long>(page_stride) * R > (1LL << 40)) return K3DA_EINVAL;
     if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return K3DA_EINVAL;
     if (qknorm) {
         if (!positions || !q_norm_w || !k_norm_w) return K3DA_EINVAL;
@@ -2002,13 +1366,13 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
     prm.scale_log2 = softmax_scale * 1.4426950408889634f;
     prm.eps = eps;
     k3da_host::rope_frequencies(prm.inv_freq, kD / 2, rope_base, yarn);
-    prm.rope_mscale = yarn != nullptr ? yarn->mscale : 1.0f;
+    prm.rope_mscale = yarn != nullptr ? k3da_host::yarn_mscale(yarn) : 1.0f;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (qknorm)
-        kSplitLaunch<true><<<prm.grid, kSplitThreads, kSplitSmem, st>>>(map, prm);
+        k3da_tc_kernel<true><<<prm.grid, kSplitThreads, kSplitSmem, st>>>(map, prm);
     else
-        kSplitLaunch<false><<<prm.grid, kSplitThreads, kSplitSmem, st>>>(map, prm);
+        k3da_tc_kernel<false><<<prm.grid, kSplitThreads, kSplitSmem, st>>>(map, prm);
     if (cudaGetLastError() != cudaSuccess) return K3DA_ECUDA;
     if (g_phase_event && cudaEventRecord(g_phase_event, st) != cudaSuccess) return K3DA_ECUDA;
     // The combine is a programmatic dependent of the split pass, so its
@@ -2036,7 +1400,7 @@ extern "C" {
 size_t k3da_workspace_bytes(int num_requests, int block_len, int num_q_heads, int num_kv_heads,
                             int page_stride) {
     if (num_requests < 1 || num_requests > kMaxR || block_len < 1 || block_len > kMaxB ||
-        !supported_heads(num_q_heads, num_kv_heads) || page_stride < 1)
+        !supported_heads(num_q_heads, num_kv_heads) || page_stride < 1 || page_stride > kMaxPageStride)
         return 0;
     return workspace_for(num_requests, num_kv_heads, page_stride);
 }
@@ -2077,7 +1441,9 @@ int k3da_attn_qknorm_noalloc(void *out, const void *qkv, const void *kv_pool, in
                              int num_requests, int block_len, int num_q_heads, int num_kv_heads, int head_dim,
                              float softmax_scale, const void *positions, int pos_dtype, const void *q_norm_w,
                              const void *k_norm_w, float eps, float rope_base, int32_t *status, void *stream) {
-    if (num_requests < 1 || num_requests > kMaxR || num_kv_heads < 1 || page_stride < 1) return K3DA_EINVAL;
+    if (num_requests < 1 || num_requests > kMaxR || num_kv_heads < 1 || page_stride < 1 ||
+        page_stride > kMaxPageStride)
+        return K3DA_EINVAL;
     if (workspace_for(num_requests, num_kv_heads, page_stride) > kStaticScratchBytes) return K3DA_EWORKSPACE;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return K3DA_ECUDA;

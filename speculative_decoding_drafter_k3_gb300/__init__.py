@@ -43,16 +43,14 @@ EXPORTED = ["k3da_workspace_bytes", "k3da_attn", "k3da_attn_qknorm", "k3da_attn_
 
 class Yarn(ctypes.Structure):
     """k3da_yarn: YaRN RoPE scaling (factor, original_max_position, beta_fast,
-    beta_slow, mscale); mscale = 0.1 ln(factor) + 1 in the YaRN paper."""
+    beta_slow, mscale).  mscale 0 asks the library for the YaRN paper's
+    default multiplier."""
     _fields_ = [("factor", ctypes.c_float), ("original_max_position", ctypes.c_float),
                 ("beta_fast", ctypes.c_float), ("beta_slow", ctypes.c_float), ("mscale", ctypes.c_float)]
 
     @classmethod
     def of(cls, factor: float, original_max_position: float, beta_fast: float = 32.0,
-           beta_slow: float = 1.0, mscale=None):
-        if mscale is None:
-            import math
-            mscale = 0.1 * math.log(factor) + 1.0
+           beta_slow: float = 1.0, mscale: float = 0.0):
         return cls(factor, original_max_position, beta_fast, beta_slow, mscale)
 
     def as_dict(self):

@@ -105,7 +105,7 @@ int launch_norm_rope(void *qkv, int num_tokens, int num_q_heads, int num_kv_head
     prm.pos_i64 = pos_dtype == K3DA_POS_I64;
     prm.eps = eps;
     k3da_host::rope_frequencies(prm.inv_freq, kD / 2, rope_base, yarn);
-    prm.mscale = yarn != nullptr ? yarn->mscale : 1.0f;
+    prm.mscale = yarn != nullptr ? k3da_host::yarn_mscale(yarn) : 1.0f;
     const long long ctas = (prm.rows + kRowsPerCta - 1) / kRowsPerCta;
     if (ctas > 0x7fffffffLL) return K3DA_EINVAL;
     k3da_norm_rope_kernel<<<static_cast<unsigned>(ctas), 32 * kRowsPerCta, 0, static_cast<cudaStream_t>(stream)>>>(

@@ -15,7 +15,15 @@ inline bool yarn_valid(const k3da_yarn *y) {
     for (float x : v)
         if (!std::isfinite(x)) return false;
     return y->factor >= 1.f && y->original_max_position > 0.f && y->beta_slow > 0.f &&
-           y->beta_fast > y->beta_slow && y->mscale > 0.f;
+           y->beta_fast > y->beta_slow && y->mscale >= 0.f;
+}
+
+// Multiplier of the rotated q and k: the caller's mscale when it is
+// positive, else the YaRN paper's sqrt(1/t) = 0.1 * ln(factor) + 1 (formed in
+// fp64, rounded once to fp32).
+inline float yarn_mscale(const k3da_yarn *y) {
+    if (y->mscale > 0.f) return y->mscale;
+    return static_cast<float>(0.1 * std::log(static_cast<double>(y->factor)) + 1.0);
 }
 
 // Frequencies of the `pairs` rotary pairs of a head of 2*pairs dims, in

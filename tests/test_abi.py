@@ -67,6 +67,7 @@ def call_attn(lib, **over):
     (dict(B=0), k3da.EINVAL),
     (dict(B=9), k3da.EINVAL),
     (dict(stride=0), k3da.EINVAL),
+    (dict(stride=1 << 25), k3da.EINVAL),        # page_stride * 64 would overflow an int
     (dict(num_pages=0), k3da.EINVAL),
     (dict(num_pages=1 << 40), k3da.EINVAL),
     (dict(scale=0.0), k3da.EINVAL),
@@ -104,6 +105,8 @@ def test_workspace_query_refuses_bad_sizes(lib):
     assert lib.k3da_workspace_bytes(8, 9, 6, 1, 32) == 0
     assert lib.k3da_workspace_bytes(8, 8, 6, 2, 32) == 0
     assert lib.k3da_workspace_bytes(8, 8, 6, 1, 0) == 0
+    assert lib.k3da_workspace_bytes(8, 8, 6, 1, 1 << 25) == 0
+    assert lib.k3da_workspace_bytes(8, 8, 6, 1, (1 << 25) - 1) > 0
 
 
 def test_workspace_size_depends_on_shapes_only(lib):
@@ -173,7 +176,7 @@ def _yarn(**over):
 
 
 @pytest.mark.parametrize("over", [dict(factor=0.5), dict(factor=float("nan")), dict(original_max_position=0.0),
-                                  dict(beta_fast=1.0), dict(beta_slow=0.0), dict(mscale=0.0),
+                                  dict(beta_fast=1.0), dict(beta_slow=0.0), dict(mscale=-1.0),
                                   dict(mscale=float("inf"))])
 def test_yarn_calls_refuse_bad_scaling(lib, over):
     y = _yarn(**over)

@@ -18,12 +18,12 @@ ours:       the CUDA library through its Python binding.  Inputs are resident
             inputs (qkv, page table, lengths, positions) copied from pinned
             host memory in one packed copy and the output copied back, inside
             the timed region.  --warm-l2 skips the flush (a warm-cache line,
-            labelled in "config").  "cpu_baseline" is the fp64 oracle on one
-            host thread (a bounded sample scaled to a call); "cpu_all_cores"
-            is one whole call of it on all host cores.
+            labelled in "config").  "cpu_baseline" is one whole call of the
+            fp64 oracle on one host thread; "cpu_all_cores" is one whole call
+            of it on all host cores.
 reference:  the fp64 CPU oracle (test infrastructure, timed as it stands on
-            the host cores), each step a bounded sample of the same workload
-            scaled to a whole call.
+            the host cores), each step one whole call of the same workload on
+            all host threads.
 
 Multi-GPU: the op does not shard across GPUs in a way that needs any
 exchange; N ranks run N independent replicas ("replicas only") and value is
@@ -197,84 +197,15 @@ def profiled_traffic(workload: str):
 
 # ------------------------------------------------------------- CPU oracle --
 
-def compact_request(case, r):
-    """Request r alone, with its pool reduced to the pages it reads (input
-    marshalling only), on the CPU."""
-    from speculative_decoding_drafter_k3_gb300 import workloads
+def cpu_baseline(case):
+    """One whole call of the fp64 oracle on one host thread (its R x Hkv
+    independent (request, kv head) units one after another), wall clock."""
+    from oracle import units as ou
 
-    sub = case.request(r)
-    L = sub.lens_list()[0]
-    n = (L + workloads.PAGE_SIZE - 1) // workloads.PAGE_SIZE
-    pages = sub.page_table[0, :n].long()
-    pool = case.pool[pages.to(case.pool.device)].cpu() if n else case.pool[:1].cpu()
-    pt = torch.full((1, max(n, 1)), -1, dtype=torch.int32)
-    pt[0, :n] = torch.arange(n, dtype=torch.int32)
-    sub.pool, sub.page_table, sub.num_pages = pool, pt, pool.shape[0]
-    return sub.to("cpu")
-
-
-def oracle_seconds(sub) -> float:
-    import oracle
-
-    t0 = time.perf_counter()
-    oracle.attn(sub.qkv, sub.pool, sub.page_table, sub.ctx_lens, num_requests=1, block_len=sub.B,
-                num_q_heads=sub.Hq, num_kv_heads=sub.Hkv, scale=sub.scale, qknorm=sub.qknorm,
-                positions=sub.positions, q_norm_w=sub.q_norm_w, k_norm_w=sub.k_norm_w,
-                eps=sub.eps, rope_base=sub.rope_base)
-    return time.perf_counter() - t0
-
-
-def cpu_baseline(case, budget_s: float = 12.0):
-    """Oracle on requests in ascending context length until ~budget_s of CPU
-    work, scaled to one call by (context + block) tokens."""
-    import oracle
-
-    oracle.build()
-    lens = case.lens_list()
-    order = sorted(range(case.R), key=lambda r: lens[r])
-    spent, tokens, used = 0.0, 0, []
-    for r in order:
-        spent += oracle_seconds(compact_request(case, r))
-        tokens += lens[r] + case.B
-        used.append(r)
-        if spent >= budget_s:
-            break
-    total = sum(L + case.B for L in lens)
-    us_per_call = spent * total / tokens * 1e6
-    return {"value": us_per_call, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": (f"fp64 C oracle, 1 thread, on requests {used} of {case.R} "
-                       f"({tokens} of {total} context+block tokens, {spent:.1f} s), "
-                       f"scaled to one call by token count")}
-
-
-def compact_unit(case, r, h):
-    """The (request r, kv head h) unit alone as numpy arrays for the oracle:
-    its q heads, k head and v head of qkv and that kv head of the request's
-    pages (input marshalling only)."""
-    import oracle
-
-    sub = compact_request(case, r)
-    G, D = case.Hq // case.Hkv, case.D
-    heads = list(range(h * G, (h + 1) * G)) + [case.Hq + h, case.Hq + case.Hkv + h]
-    qkv = sub.qkv.view(case.B, case.Hq + 2 * case.Hkv, D)[:, heads].reshape(case.B, (G + 2) * D)
-    pool = sub.pool[:, :, h:h + 1].contiguous()
-    unit = {"qkv": oracle.bf16_bits(qkv), "pool": oracle.bf16_bits(pool),
-            "page_table": sub.page_table.numpy(), "ctx_lens": sub.ctx_lens.numpy(),
-            "G": G, "B": case.B, "scale": case.scale, "qknorm": case.qknorm,
-            "tokens": sub.lens_list()[0] + case.B}
-    if case.qknorm:
-        unit.update(positions=sub.positions.numpy(), q_norm_w=oracle.bf16_bits(sub.q_norm_w),
-                    k_norm_w=oracle.bf16_bits(sub.k_norm_w), eps=case.eps, rope_base=case.rope_base)
-    return unit
-
-
-def _oracle_unit(u):
-    import oracle
-
-    return oracle.attn(u["qkv"], u["pool"], u["page_table"], u["ctx_lens"], num_requests=1, block_len=u["B"],
-                num_q_heads=u["G"], num_kv_heads=1, scale=u["scale"], qknorm=u["qknorm"],
-                positions=u.get("positions"), q_norm_w=u.get("q_norm_w"), k_norm_w=u.get("k_norm_w"),
-                eps=u.get("eps", 1e-5), rope_base=u.get("rope_base", 10000.0))
+    us = ou.units_of(case)
+    _, wall, n = ou.run_units(us, threads=1)
+    return {"value": wall * 1e6, "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": f"whole call: fp64 C oracle, {len(us)} (request, kv head) units on 1 thread, wall clock"}
 
 
 def cpu_all_cores(case, threads: int = 0):
@@ -283,20 +214,12 @@ def cpu_all_cores(case, threads: int = 0):
     threads (the C oracle keeps no global state and ctypes releases the GIL
     during each call).  Wall-clock time of the pool; inputs marshalled
     before the clock starts."""
-    from concurrent.futures import ThreadPoolExecutor
-    import oracle
+    from oracle import units as ou
 
-    oracle.build()
-    n = threads or len(os.sched_getaffinity(0))
-    units = sorted((compact_unit(case, r, h) for r in range(case.R) for h in range(case.Hkv)),
-                   key=lambda u: -u["tokens"])
-    with ThreadPoolExecutor(max_workers=n) as ex:
-        list(ex.map(lambda _: None, range(n)))  # threads started before the clock
-        t0 = time.perf_counter()
-        list(ex.map(_oracle_unit, units))
-        wall = time.perf_counter() - t0
+    us = ou.units_of(case)
+    _, wall, n = ou.run_units(us, threads=threads)
     return {"value": wall * 1e6, "unit": UNIT, "cores": n, "kind": "oracle",
-            "sample": (f"fp64 C oracle, one whole call: {len(units)} (request, kv head) units on "
+            "sample": (f"whole call: fp64 C oracle, {len(us)} (request, kv head) units on "
                        f"{n} threads, wall clock")}
 
 
@@ -316,31 +239,33 @@ def config_of(case, extra=None):
 
 
 def run_reference(args, world, rank):
+    """The reference arm: the fp64 CPU oracle, as it stands, on the host
+    cores.  Each step is one whole call of the workload (its (request, kv
+    head) units on a pool of all host threads), wall clock."""
     from speculative_decoding_drafter_k3_gb300 import workloads
-    import oracle
+    from oracle import units as ou
 
     if rank != 0:
         return
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     case = workloads.WORKLOADS[args.workload](device=dev)
-    oracle.build()
-    lens = case.lens_list()
-    r = min(range(case.R), key=lambda i: lens[i])
-    sub = compact_request(case, r)
-    scale = sum(L + case.B for L in lens) / (lens[r] + case.B)
+    us = ou.units_of(case)
     for _ in range(args.warmup):
-        oracle_seconds(sub)
-    times = [oracle_seconds(sub) * scale for _ in range(args.steps)]
-    us = statistics.mean(times) * 1e6
-    sample = (f"fp64 C oracle, 1 thread, request {r} of {case.R} ({lens[r]}+{case.B} tokens) per "
-              f"step, scaled to one call by context+block tokens (x{scale:.2f})")
-    line = {"impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
+        ou.run_units(us)
+    times, n = [], 0
+    for _ in range(args.steps):
+        _, wall, n = ou.run_units(us)
+        times.append(wall)
+    us_call = statistics.mean(times) * 1e6
+    sample = (f"whole call per step: fp64 C oracle, {len(us)} (request, kv head) units on {n} host "
+              f"threads, wall clock")
+    line = {"impl": "reference", "metric": METRIC, "value": us_call, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": us_call / 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_of(case),
-            "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": us_call, "unit": UNIT, "cores": n, "kind": "oracle",
                              "sample": sample},
-            "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": us_call, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
@@ -357,7 +282,7 @@ def run_ours(args, world, rank):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    sink = torch.empty(1, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
 
     class _Flush:
         @staticmethod

@@ -1,35 +1,61 @@
-"""Properties the pages' tests ask of the op beyond parity: no NaN, the pool
-left byte-untouched, bit-identical reruns, isolated requests, device-side
-range checks that flag and never fault, a poisoned workspace, poisoned
-page-table tails and pool slots, and CUDA-graph replay with rewritten
-lengths, page table, qkv and positions."""
+"""Properties the pages' tests ask of the op beyond parity (page "[None][feat]
+Share Kimi K3 FP4 modeling and add NVFP4 support on SM103", NVIDIA/
+TensorRT-LLM PR #20532, the drafter-attention commit's test list): no NaN,
+the pool left byte-untouched, bit-identical reruns, isolated requests,
+device-side range checks that flag and never fault, a poisoned workspace,
+poisoned page-table tails and pool slots, and CUDA-graph replay with
+rewritten lengths, page table, qkv and positions.  Reruns, the pool and
+graph replay are checked on every workload of the op: the tiny plain call,
+the 8x8 mixed-length and 24/4 strided cases, all eight request x token
+splits and the long-context stress case."""
+import functools
+
 import numpy as np
 import pytest
 import torch
 
 import speculative_decoding_drafter_k3_gb300 as k3da
+from oracle import units as ou
 from speculative_decoding_drafter_k3_gb300 import workloads
 from common import assert_close, oracle_for
 
 pytestmark = pytest.mark.gpu
+
+CONFIGS = dict([("tiny", workloads.tiny), ("mixed_8x8", workloads.mixed_8x8),
+                ("heads_24_4", workloads.heads_24_4)]
+               + [(f"split_{R}x{B}", functools.partial(workloads.split_sweep, R, B)) for R, B in workloads.SPLITS]
+               + [("long_context", workloads.long_context)])
 
 
 def fresh_out(case):
     return torch.empty(case.T, case.Hq * case.D, dtype=torch.bfloat16, device="cuda")
 
 
-def test_reruns_are_bit_identical_and_pool_untouched():
-    case = workloads.heads_24_4(device="cuda")
+def whole_oracle(case):
+    """The oracle on the whole call; the long-context case runs unit by unit
+    on all host cores."""
+    if case.context_tokens() > 100000:
+        return ou.oracle_call(case)
+    return oracle_for(case)
+
+
+@pytest.mark.parametrize("config", sorted(CONFIGS))
+def test_reruns_are_bit_identical_and_pool_untouched(config):
+    case = CONFIGS[config](device="cuda")
     pool_before = case.pool.clone()
     ws = k3da.case_workspace(case)
-    a = k3da.run_case(case, workspace=ws).clone()
-    for _ in range(5):
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a = k3da.run_case(case, workspace=ws, status=status).clone()
+    for _ in range(3):
         ws.fill_(0xFF)  # NaN-pattern workspace between calls
-        b = k3da.run_case(case, workspace=ws)
+        b = k3da.run_case(case, workspace=ws, status=status)
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     torch.cuda.synchronize()
+    assert int(status.item()) == 0
     assert torch.equal(case.pool.view(torch.int16), pool_before.view(torch.int16))
     assert torch.isfinite(a.float()).all()
+    if config != "long_context":  # parity of the long-context case: test_parity
+        assert_close(a, oracle_for(case), config)
 
 
 def test_requests_are_isolated():
@@ -112,31 +138,43 @@ def test_host_side_refusals_raise():
                        block_len=case.B, num_q_heads=8, num_kv_heads=1, workspace=ws)
 
 
-@pytest.mark.parametrize("maker", [workloads.mixed_8x8, workloads.heads_24_4])
-def test_graph_replay_with_rewritten_inputs(maker):
+@pytest.mark.parametrize("config", sorted(CONFIGS))
+def test_graph_replay_with_rewritten_inputs(config):
+    """One call captured in a CUDA graph, then replayed after qkv, lengths,
+    page table and positions (the fused variants) were rewritten in place:
+    every replay equals an eager call bit for bit and the oracle element by
+    element."""
+    maker = CONFIGS[config]
     case = maker(device="cuda")
     ws = k3da.case_workspace(case)
     out = fresh_out(case)
-    k3da.run_case(case, out=out, workspace=ws)  # first call outside capture
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k3da.run_case(case, out=out, workspace=ws, status=status)  # first call outside capture
     torch.cuda.synchronize()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        k3da.run_case(case, out=out, workspace=ws, stream=s)
-    for seed in [11, 12, 13]:
+        k3da.run_case(case, out=out, workspace=ws, status=status, stream=s)
+    seeds = [11, 12] if config == "long_context" else [11, 12, 13]
+    for seed in seeds:
         new = maker(device="cuda", seed=seed)
         case.qkv.copy_(new.qkv)
         case.ctx_lens.copy_(new.ctx_lens)
         case.page_table.copy_(new.page_table)
-        case.positions.copy_(new.positions)
+        if case.positions is not None:
+            case.positions.copy_(new.positions)
+        del new
+        ws.fill_(0xFF)
         g.replay()
         torch.cuda.synchronize()
         replayed = out.clone()
-        eager = k3da.run_case(case, workspace=ws)
+        eager = k3da.run_case(case, workspace=ws, status=status)
         torch.cuda.synchronize()
+        assert int(status.item()) == 0
         assert torch.equal(replayed.view(torch.int16), eager.view(torch.int16))
-        assert_close(replayed, oracle_for(case), f"replay seed {seed}")
+        if config != "long_context" or seed == seeds[-1]:
+            assert_close(replayed, whole_oracle(case), f"{config} replay seed {seed}")
 
 
 def test_a_stuck_wait_times_out_with_a_status_and_the_context_survives():

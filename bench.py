@@ -70,6 +70,8 @@ def parse():
     ap.add_argument("--heads", choices=["6/1", "24/4"], default="24/4")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-small", action="store_true",
+                    help="skip the extra timing of the small workloads on the default line")
     ap.add_argument("--warm-l2", action="store_true",
                     help="do not flush L2 between timed calls (a labelled warm-cache line, "
                          "never the headline)")
@@ -303,30 +305,33 @@ def run_ours(args, world, rank):
 
     yarn = k3da.Yarn.of(4.0, 4096.0) if args.yarn and case.qknorm else None
 
-    def call():
-        k3da.run_case(case, out=out, workspace=ws, status=status, yarn=yarn)
-
-    for _ in range(max(args.warmup, 3)):
-        flush.zero_()
-        call()
-    torch.cuda.synchronize()
+    def timed_calls(c, o, w, K):
+        """K calls of case c, each after an L2 flush, each bracketed by CUDA
+        events on the launching stream; returns the per-call times in ms."""
+        for _ in range(max(args.warmup, 3)):
+            flush.zero_()
+            k3da.run_case(c, out=o, workspace=w, status=status, yarn=yarn)
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record()
+            k3da.run_case(c, out=o, workspace=w, status=status, yarn=yarn)
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        barrier(world)
+        return [e[0].elapsed_time(e[1]) for e in ev]
 
     K = args.steps
     # Headline: whole calls (split pass + combine), one event pair per call.
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     clocks = ClockSampler(dev.index) if rank == 0 else None
-    barrier(world)
-    torch.cuda.synchronize()
-    for i in range(K):
-        flush.zero_()
-        ev[i][0].record()
-        call()
-        ev[i][1].record()
-    torch.cuda.synchronize()
-    barrier(world)
+    call_ms = timed_calls(case, out, ws, K)
     clock_info = clocks.stop() if clocks else None
-    call_ms = [e[0].elapsed_time(e[1]) for e in ev]
     total_ms = max_over_ranks(sum(call_ms), world)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    value = total_ms * 1e3 / (K * world)
 
     # Roofline: the split pass alone, bracketed by an event the library
     # records between its two kernels.
@@ -338,14 +343,26 @@ def run_ours(args, world, rank):
         flush.zero_()
         pev[i][0].record()
         k3da.set_phase_event(pev[i][1])
-        call()
+        k3da.run_case(case, out=out, workspace=ws, status=status, yarn=yarn)
         pev[i][2].record()
     torch.cuda.synchronize()
     k3da.set_phase_event(None)
     split_ms = [e[0].elapsed_time(e[1]) for e in pev]
     combine_ms = [e[1].elapsed_time(e[2]) for e in pev]  # combine after the event: no launch overlap
-    assert int(status.item()) == 0, f"device status {int(status.item())}"
-    value = total_ms * 1e3 / (K * world)
+
+    # The drafter's deployed shapes (8x8 mixed lengths, 24/4 heads, the W=6
+    # block), timed the same way in the same process.
+    small = None
+    if args.workload == "long_context" and not args.no_small:
+        small = {}
+        for name in ("mixed_8x8", "heads_24_4", "w6_8x6"):
+            c = workloads.WORKLOADS[name](device=dev)
+            o = torch.empty(c.T, c.Hq * c.D, dtype=torch.bfloat16, device=dev)
+            ms = timed_calls(c, o, k3da.case_workspace(c), K)
+            small[name] = {"us_per_call": statistics.mean(ms) * 1e3,
+                           "median_us": statistics.median(ms) * 1e3,
+                           "algorithmic_bytes": c.algorithmic_bytes()}
+        assert int(status.item()) == 0, f"device status {int(status.item())}"
 
     # End to end through the public binding with host buffers: the step's
     # inputs (qkv, page table, lengths, positions) travel from pinned host
@@ -406,7 +423,8 @@ def run_ours(args, world, rank):
                 "algorithmic_bytes_per_launch": split_bytes, "launch_us": split_us,
                 "peak_source": peak_src,
                 "combine_us_unoverlapped": statistics.mean(combine_ms) * 1e3,
-                "whole_call_gbs": case.algorithmic_bytes() / (value * 1e-6) / 1e9}
+                "whole_call_gbs": case.algorithmic_bytes() / (value * 1e-6) / 1e9,
+                "whole_call_frac": case.algorithmic_bytes() / (value * 1e-6) / 1e9 / peak}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": False,
@@ -418,6 +436,7 @@ def run_ours(args, world, rank):
                                        "rope": "yarn(4.0, 4096, 32, 1)" if yarn is not None else "neox",
                                        "split_ctas": k3da.split_grid(dev.index)}),
             "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clock_info,
+            "small_workloads": small,
             "median_call_us": statistics.median(call_ms) * 1e3,
             "p10_p90_call_us": [sorted(call_ms)[int(0.1 * (K - 1))] * 1e3,
                                 sorted(call_ms)[int(0.9 * (K - 1))] * 1e3]}

@@ -251,6 +251,10 @@ __device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool repor
         const int ch16 = (items + kChunkSplits - 1) / kChunkSplits;
         const int floor_ch = ch16 < 4 ? ch16 : 4;
         ch = ch > floor_ch ? ch : floor_ch;
+        // Chunks of 5 or more pages take the next power of two (8, 16, 32),
+        // so the chunk sizes of long units divide one another and a CTA's
+        // share of the item line holds whole chunks of any of them.
+        if (ch > 4) ch = 1 << (32 - __clz(ch - 1));
         ch = ch < 1 ? 1 : (ch > kChunkMax ? kChunkMax : ch);
         nch = (items + ch - 1) / ch;
     }
@@ -278,13 +282,42 @@ __device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool repor
         pl->nrun = 0;
     }
     if (cta < 0) return;
-    const long long lo = ceil_div_ll(static_cast<long long>(cta) * W, C);
-    const long long hi = ceil_div_ll(static_cast<long long>(cta + 1) * W, C);
+    // Which CTA computes which chunk.  With few items per CTA (W < 2 C
+    // chmax, chmax the largest chunk), CTA c takes the chunks whose first
+    // item lies in the c-th of C equal slices of the item line.  With many
+    // (every CTA holds several of the largest chunks), whole chunks would
+    // leave some CTAs one chunk more than others and a tail in which only
+    // those run; instead each chunk counts as its unit's chunk size ch
+    // (the short last chunk too) on a nominal line of WN = sum nch * ch,
+    // cut for Ce = ceil(WN / (k chmax)) CTAs with k = ceil(WN / (C chmax)):
+    // every CTA then holds k chunks' worth (chunk sizes are powers of two,
+    // so the slices hold whole chunks) and all stream to the end together;
+    // CTAs c >= Ce take no work.  Either way a function of the lengths that
+    // only decides which CTA computes a chunk, never a chunk's boundaries.
+    int chmax = u < U ? ch : 1;
+    long long sw = u < U ? static_cast<long long>(nch) * ch : 0;  // nominal line, inclusive scan
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) chmax = max(chmax, __shfl_xor_sync(kFull, chmax, off));
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long t = __shfl_up_sync(kFull, sw, off);
+        if (lane >= off) sw += t;
+    }
+    const long long WN = __shfl_sync(kFull, sw, U - 1);
+    long long Ce = C, line_base = base, line_total = W;
+    if (W >= 2LL * C * chmax) {
+        const long long k = ceil_div_ll(WN, static_cast<long long>(C) * chmax);
+        Ce = ceil_div_ll(WN, k * chmax);
+        line_base = sw - (u < U ? static_cast<long long>(nch) * ch : 0);
+        line_total = WN;
+    }
+    const long long lo = ceil_div_ll(static_cast<long long>(cta) * line_total, Ce);
+    const long long hi = ceil_div_ll(static_cast<long long>(cta + 1) * line_total, Ce);
     bool has = false;
     int j0 = 0, j1 = 0, p0 = 0, npg = 0;
-    if (u < U) {
-        long long a = lo - base <= 0 ? 0 : ceil_div_ll(lo - base, ch);
-        long long b = hi - base <= 0 ? 0 : ceil_div_ll(hi - base, ch);
+    if (u < U && cta < Ce) {
+        long long a = lo - line_base <= 0 ? 0 : ceil_div_ll(lo - line_base, ch);
+        long long b = hi - line_base <= 0 ? 0 : ceil_div_ll(hi - line_base, ch);
         a = a > nch ? nch : a;
         b = b > nch ? nch : b;
         if (a < b) {

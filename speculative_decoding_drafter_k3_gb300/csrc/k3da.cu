@@ -79,7 +79,6 @@ struct Params {
     const void *positions;
     const __nv_bfloat16 *q_w;
     const __nv_bfloat16 *k_w;
-    int *ws_units;      // [2][32]: first chunk slot and chunk count of each unit
     __nv_bfloat16 *ws_o;  // [slots][48][64]: a chunk's unnormalised O, rounded to bf16 once
     float2 *ws_ml;      // [slots][48]  (m in log2 units, l)
     int32_t *status;
@@ -88,6 +87,7 @@ struct Params {
     int R, B, Hq, Hkv;
     int pos_i64;
     int grid;           // CTAs of the split pass
+    int slots_per_unit; // workspace slots of a unit: chunk j of unit u is slot u * slots_per_unit + j
     float scale_log2;   // softmax_scale * log2(e)
     float eps;
     float rope_mscale;  // multiplier of the rotated q and k (YaRN), 1 for plain RoPE
@@ -191,7 +191,7 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 // Items of unit u = r*Hkv + h: 1 (the block) + ceil(L_r/64) (pages); unit u
 // covers items [ustart[u], ustart[u+1]) of the line, W = ustart[U].  Chunk j
 // of unit u covers its items [j*ch, min((j+1)*ch, items)) and leaves its
-// partial in workspace slot cstart[u] + j.  CTA c of C takes the chunks whose
+// partial in workspace slot u * slots_per_unit + j.  CTA c of C takes the chunks whose
 // first item lies in [ceil(c*W/C), ceil((c+1)*W/C)): one run of consecutive
 // chunks per unit it touches.
 
@@ -220,6 +220,32 @@ __host__ __device__ constexpr int chunk_splits(int units) {
     return (kChunkTarget + units - 1) / units > kChunkSplits ? (kChunkTarget + units - 1) / units : kChunkSplits;
 }
 
+// Chunk size and count of a unit of `items` items (the block and its
+// pages) in a call of U units: a function of the unit's own length and the
+// call's shape only, so a chunk's partial does not depend on other requests.
+// Finer chunks for few units, but never below the 16-way split's chunk or 4
+// items, whichever is smaller (short units keep the 16-way chunking); chunks
+// of 5 or more items take the next power of two (8, 16, 32), so the chunk
+// sizes of long units divide one another.
+__device__ __forceinline__ void unit_chunking(int items, int U, int &ch, int &nch) {
+    const int splits = chunk_splits(U);
+    ch = (items + splits - 1) / splits;
+    const int ch16 = (items + kChunkSplits - 1) / kChunkSplits;
+    const int floor_ch = ch16 < 4 ? ch16 : 4;
+    ch = ch > floor_ch ? ch : floor_ch;
+    if (ch > 4) ch = 1 << (32 - __clz(ch - 1));
+    ch = ch < 1 ? 1 : (ch > kChunkMax ? kChunkMax : ch);
+    nch = (items + ch - 1) / ch;
+}
+
+// A request's context length, clamped to [0, page_stride * 64] (a length
+// outside it is flagged by the split pass).
+__device__ __forceinline__ int clamped_length(const Params &p, int L, bool *bad) {
+    const int cap = p.page_stride * kP;
+    *bad = L < 0 || L > cap;
+    return L < 0 ? 0 : (L > cap ? cap : L);
+}
+
 // Warp 0 reads and checks ctx_lens and builds the plan, one lane per unit
 // with shuffle scans.  The caller syncs.  An item is the block (item 0) or
 // one page of the unit; a chunk holds at most kChunkMax items.
@@ -228,11 +254,8 @@ __device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool repor
     const int lane = threadIdx.x;
     int L = 0;
     if (lane < p.R) {
-        L = __ldg(p.ctx_lens + lane);
-        const int cap = p.page_stride * kP;
         bool bad = false;
-        if (L < 0) { L = 0; bad = true; }
-        if (L > cap) { L = cap; bad = true; }
+        L = clamped_length(p, __ldg(p.ctx_lens + lane), &bad);
         if (bad && report && p.status) atomicOr(p.status, K3DA_STATUS_BAD_LENGTH);
         pl->lens[lane] = L;
     }
@@ -240,23 +263,10 @@ __device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool repor
     const int u = lane;
     const int Lu = __shfl_sync(kFull, L, (u < U ? u / p.Hkv : 0));
     int items = 0, ch = 1, nch = 0, npages = 0;
-    const int splits = chunk_splits(U);
     if (u < U) {
         npages = (Lu + kP - 1) / kP;
         items = 1 + npages;
-        // Finer chunks for few units, but never below the 16-way split's
-        // chunk or 4 items, whichever is smaller: short units keep the
-        // chunking of the 16-way split.
-        ch = (items + splits - 1) / splits;
-        const int ch16 = (items + kChunkSplits - 1) / kChunkSplits;
-        const int floor_ch = ch16 < 4 ? ch16 : 4;
-        ch = ch > floor_ch ? ch : floor_ch;
-        // Chunks of 5 or more pages take the next power of two (8, 16, 32),
-        // so the chunk sizes of long units divide one another and a CTA's
-        // share of the item line holds whole chunks of any of them.
-        if (ch > 4) ch = 1 << (32 - __clz(ch - 1));
-        ch = ch < 1 ? 1 : (ch > kChunkMax ? kChunkMax : ch);
-        nch = (items + ch - 1) / ch;
+        unit_chunking(items, U, ch, nch);
     }
     long long si = items;  // inclusive scans over units
     int sn = nch;
@@ -550,12 +560,6 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     fence_after();
     const uint32_t tmem = *taddr_slot;
     const int nrun = pl->nrun;
-    if (blockIdx.x == 0 && threadIdx.x < p.R * p.Hkv) {
-        // The combine reads each unit's chunk slots from here instead of
-        // rebuilding the plan.
-        p.ws_units[threadIdx.x] = pl->cstart[threadIdx.x];
-        p.ws_units[kMaxUnits + threadIdx.x] = pl->nch[threadIdx.x];
-    }
 
     if (warp == kProducerWarp && nrun > 0) {
         // ------------------------------------------------ producer warp --
@@ -1007,7 +1011,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                 }
                 // ---- chunk partial: written during the next item (or below).
                 epi_pending = true;
-                epi_slot = static_cast<long long>(pl->cstart[u]) + jc;
+                epi_slot = static_cast<long long>(u) * p.slots_per_unit + jc;
                 epi_m = m_used;
                 epi_l = lsum;
             }
@@ -1033,46 +1037,51 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
 //
 // One CTA per (unit, 2 query rows), 128 threads: thread = (row, 8 dims,
 // chunk lane sg of 8), the 8 chunk lanes of one (row, dims) adjacent in a
-// warp.  Lane sg folds the unit's chunk partials sg, sg+8, ... online,
-// loading kCombineFold of them at once; the lanes then merge by a fixed
-// butterfly of shuffles, so the result depends on nothing but the unit's
-// own chunks.  The unit's chunk slots come from the table the split pass
-// writes.  Launched as a programmatic dependent of the split pass:
-// griddepcontrol.wait orders every workspace read after it.
+// warp.  Lane sg folds the unit's chunk partials sg, sg+8, ... online; it
+// issues the loads of up to kCombineFold of them at once, so a unit of up to
+// 72 chunks is read in one round trip; the lanes then merge by a fixed
+// butterfly of shuffles, so the result depends on nothing but the unit's own
+// chunks.  Launched as a programmatic dependent of the split pass: the
+// unit's chunk count comes from its context length (an input, read before
+// griddepcontrol.wait while the split pass still runs), its partials sit at
+// fixed slots, and griddepcontrol.wait orders every workspace read after
+// the split pass.
 constexpr int kCombineRows = 2;
 constexpr int kCombineLanes = 8;
-constexpr int kCombineFold = 4;
+constexpr int kCombineFold = 9;
 
-__global__ void __launch_bounds__(128) k3da_combine_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(128, 6) k3da_combine_kernel(const __grid_constant__ Params p) {
     const int per_unit = kRows / kCombineRows;
     const int u = blockIdx.x / per_unit;
     const int row = (blockIdx.x - u * per_unit) * kCombineRows + (threadIdx.x >> 6);
     const int dc = (threadIdx.x >> 3) & 7, sg = threadIdx.x & (kCombineLanes - 1);
     const int rows = kG * p.B;
     if ((blockIdx.x - u * per_unit) * kCombineRows >= rows) return;  // whole CTA
+    const int r = u / p.Hkv, h = u - r * p.Hkv;
+    bool bad;
+    const int L = clamped_length(p, __ldg(p.ctx_lens + r), &bad);
+    int ch, nch;
+    unit_chunking(1 + (L + kP - 1) / kP, p.R * p.Hkv, ch, nch);
+    const uint8_t *slots = reinterpret_cast<const uint8_t *>(p.ws_o) +
+                           static_cast<long long>(u) * p.slots_per_unit * kPartialElems * 2;
+    const float2 *mls = p.ws_ml + static_cast<long long>(u) * p.slots_per_unit * kRows;
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const long long slot0 = p.ws_units[u];
-    const int nch = p.ws_units[kMaxUnits + u];
     float m = -INFINITY, l = 0.f;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (row < rows) {
         for (int base = 0; base < nch; base += kCombineLanes * kCombineFold) {
             float2 ml[kCombineFold];
-            float4 v0[kCombineFold], v1[kCombineFold];
+            uint4 w[kCombineFold];
 #pragma unroll
             for (int f = 0; f < kCombineFold; ++f) {
                 const int j = base + sg + f * kCombineLanes;
                 if (j < nch) {
-                    const long long slot = slot0 + j;
-                    ml[f] = p.ws_ml[slot * kRows + row];
-                    const uint4 w = *reinterpret_cast<const uint4 *>(p.ws_o + slot * kPartialElems + row * kD + dc * 8);
-                    v0[f] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
-                                        __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
-                    v1[f] = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
-                                        __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+                    ml[f] = mls[static_cast<long long>(j) * kRows + row];
+                    w[f] = *reinterpret_cast<const uint4 *>(slots + (static_cast<long long>(j) * kPartialElems +
+                                                                     row * kD + dc * 8) * 2);
                 } else {
                     ml[f] = make_float2(-INFINITY, 0.f);
-                    v0[f] = v1[f] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    w[f] = make_uint4(0, 0, 0, 0);
                 }
             }
 #pragma unroll
@@ -1082,14 +1091,12 @@ __global__ void __launch_bounds__(128) k3da_combine_kernel(const __grid_constant
                 const float fo = exp2_approx(m - mm), fn = exp2_approx(ml[f].x - mm);
                 m = mm;
                 l = l * fo + ml[f].y * fn;
-                acc[0] = acc[0] * fo + v0[f].x * fn;
-                acc[1] = acc[1] * fo + v0[f].y * fn;
-                acc[2] = acc[2] * fo + v0[f].z * fn;
-                acc[3] = acc[3] * fo + v0[f].w * fn;
-                acc[4] = acc[4] * fo + v1[f].x * fn;
-                acc[5] = acc[5] * fo + v1[f].y * fn;
-                acc[6] = acc[6] * fo + v1[f].z * fn;
-                acc[7] = acc[7] * fo + v1[f].w * fn;
+                const uint32_t v[4] = {w[f].x, w[f].y, w[f].z, w[f].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc[2 * e] = acc[2 * e] * fo + __uint_as_float(v[e] << 16) * fn;
+                    acc[2 * e + 1] = acc[2 * e + 1] * fo + __uint_as_float(v[e] & 0xffff0000u) * fn;
+                }
             }
         }
     }
@@ -1111,7 +1118,6 @@ __global__ void __launch_bounds__(128) k3da_combine_kernel(const __grid_constant
     }
     if (sg == 0 && row < rows) {
         const float inv = 1.0f / l;
-        const int r = u / p.Hkv, h = u - r * p.Hkv;
         const int g = row / p.B, ti = row - g * p.B;
         const long long t = static_cast<long long>(r) * p.B + ti;
         uint4 packed;
@@ -1273,12 +1279,15 @@ bool supported_heads(int hq, int hkv) { return (hq == 6 && hkv == 1) || (hq == 2
 
 // Chunks a unit can have: at most chunk_splits(R*Hkv), or ceil(items/ch_max)
 // once chunks reach ch_max = kChunkMax items; items <= 1 + page_stride.
-constexpr size_t workspace_slots(int R, int Hkv, int page_stride) {
+constexpr long long slots_per_unit(int R, int Hkv, int page_stride) {
     const long long items = 1 + static_cast<long long>(page_stride);
     const long long by_len = (items + kChunkMax - 1) / kChunkMax;
     const long long splits = chunk_splits(R * Hkv);
-    const long long per_unit = by_len > splits ? by_len : splits;
-    return static_cast<size_t>(R) * Hkv * static_cast<size_t>(per_unit);
+    return by_len > splits ? by_len : splits;
+}
+
+constexpr size_t workspace_slots(int R, int Hkv, int page_stride) {
+    return static_cast<size_t>(R) * Hkv * static_cast<size_t>(slots_per_unit(R, Hkv, page_stride));
 }
 
 constexpr size_t kWsHeaderBytes = 512;  // unit table, then the partials (16-byte aligned)
@@ -1383,7 +1392,7 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
     prm.q_w = static_cast<const __nv_bfloat16 *>(q_norm_w);
     prm.k_w = static_cast<const __nv_bfloat16 *>(k_norm_w);
     const size_t slots = workspace_slots(R, Hkv, page_stride);
-    prm.ws_units = static_cast<int *>(workspace);
+    prm.slots_per_unit = static_cast<int>(slots_per_unit(R, Hkv, page_stride));
     prm.ws_o = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(workspace) + kWsHeaderBytes);
     prm.ws_ml = reinterpret_cast<float2 *>(prm.ws_o + slots * kPartialElems);
     prm.status = status;

@@ -32,6 +32,7 @@ the job's aggregate time per call (max-over-ranks time / calls of all ranks).
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -154,6 +155,24 @@ class ClockSampler:
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def samples(self) -> int:
+        if self.proc is None:
+            return 0
+        try:
+            return sum(1 for _ in open(self.path))
+        except OSError:
+            return 0
+
+    def settle(self, busy, seconds: float = 0.8):
+        """Keeps the GPU busy (untimed calls of ``busy``) until nvidia-smi has
+        been sampling for ``seconds``, so its start-up never overlaps the
+        timed region and the samples it takes are under load."""
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds or (self.proc is not None and self.samples() < 2
+                                                      and time.perf_counter() - t0 < 5.0):
+            busy()
+            torch.cuda.synchronize()
 
     def stop(self):
         if self.proc is None:
@@ -305,29 +324,41 @@ def run_ours(args, world, rank):
 
     yarn = k3da.Yarn.of(4.0, 4096.0) if args.yarn and case.qknorm else None
 
-    def timed_calls(c, o, w, K):
+    def timed_calls(c, o, w, K, clocks=None):
         """K calls of case c, each after an L2 flush, each bracketed by CUDA
-        events on the launching stream; returns the per-call times in ms."""
+        events on the launching stream; returns the per-call times in ms.
+        Python's garbage collector is off while the calls are enqueued, so
+        no host pause can open a gap between an event and its call."""
         for _ in range(max(args.warmup, 3)):
             flush.zero_()
             k3da.run_case(c, out=o, workspace=w, status=status, yarn=yarn)
         torch.cuda.synchronize()
+        if clocks is not None:
+            def busy():
+                for _ in range(20):
+                    flush.zero_()
+                    k3da.run_case(c, out=o, workspace=w, status=status, yarn=yarn)
+            clocks.settle(busy)
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
         barrier(world)
         torch.cuda.synchronize()
-        for i in range(K):
-            flush.zero_()
-            ev[i][0].record()
-            k3da.run_case(c, out=o, workspace=w, status=status, yarn=yarn)
-            ev[i][1].record()
-        torch.cuda.synchronize()
+        gc.disable()
+        try:
+            for i in range(K):
+                flush.zero_()
+                ev[i][0].record()
+                k3da.run_case(c, out=o, workspace=w, status=status, yarn=yarn)
+                ev[i][1].record()
+            torch.cuda.synchronize()
+        finally:
+            gc.enable()
         barrier(world)
         return [e[0].elapsed_time(e[1]) for e in ev]
 
     K = args.steps
     # Headline: whole calls (split pass + combine), one event pair per call.
     clocks = ClockSampler(dev.index) if rank == 0 else None
-    call_ms = timed_calls(case, out, ws, K)
+    call_ms = timed_calls(case, out, ws, K, clocks)
     clock_info = clocks.stop() if clocks else None
     total_ms = max_over_ranks(sum(call_ms), world)
     assert int(status.item()) == 0, f"device status {int(status.item())}"
@@ -339,6 +370,7 @@ def run_ours(args, world, rank):
     for e in pev:
         e[1].record()  # torch creates its events lazily: create the one the library records
     torch.cuda.synchronize()
+    gc.disable()
     for i in range(K):
         flush.zero_()
         pev[i][0].record()
@@ -346,6 +378,7 @@ def run_ours(args, world, rank):
         k3da.run_case(case, out=out, workspace=ws, status=status, yarn=yarn)
         pev[i][2].record()
     torch.cuda.synchronize()
+    gc.enable()
     k3da.set_phase_event(None)
     split_ms = [e[0].elapsed_time(e[1]) for e in pev]
     combine_ms = [e[1].elapsed_time(e[2]) for e in pev]  # combine after the event: no launch overlap
@@ -399,12 +432,14 @@ def run_ours(args, world, rank):
         eev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
         barrier(world)
         torch.cuda.synchronize()
+        gc.disable()
         for i in range(K):
             flush.zero_()
             eev[i][0].record()
             step_e2e()
             eev[i][1].record()
         torch.cuda.synchronize()
+        gc.enable()
         barrier(world)
         e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in eev), world)
         e2e = {"value": e2e_ms * 1e3 / (K * world), "unit": UNIT,

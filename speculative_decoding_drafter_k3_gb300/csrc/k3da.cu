@@ -32,8 +32,9 @@
 //     rescale) and hand P to the P.V product through TMEM.
 //   * When a CTA starts on a unit, its q (and block k, v) rows are staged
 //     with one batch of cp.async copies and turned into operand tiles:
-//     RMSNorm and RoPE happen on the way in, RoPE angles are reduced in fp64
-//     then turned by an accurate sincosf.
+//     RMSNorm and RoPE happen on the way in.  A RoPE angle is reduced
+//     exactly in integer arithmetic (position times a 64-bit fixed-point
+//     turn rate, wrapping), then turned by an accurate sincospif.
 //   * Each chunk leaves an unnormalised partial (O as bf16, m and l in fp32)
 //     in the workspace; the combine kernel folds a unit's chunk partials in
 //     a fixed order and writes bf16 out, so reruns are bit-identical.
@@ -88,10 +89,11 @@ struct Params {
     int pos_i64;
     int grid;           // CTAs of the split pass
     int slots_per_unit; // workspace slots of a unit: chunk j of unit u is slot u * slots_per_unit + j
+    int splits;         // chunk_splits(R * Hkv)
     float scale_log2;   // softmax_scale * log2(e)
     float eps;
     float rope_mscale;  // multiplier of the rotated q and k (YaRN), 1 for plain RoPE
-    double inv_freq[kD / 2];
+    unsigned long long turn_rate[kD / 2];  // RoPE frequency of pair j in turns per position, 2^64 = one turn
 };
 
 // ------------------------------------------------------------ PTX helpers --
@@ -180,6 +182,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Global stores with an L2 cache-policy hint (the chunk partials: kept in L2
+// for the combine while the pool streams through with evict_first).
+__device__ __forceinline__ void st_hint_v4(uint4 *p, uint4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_hint_f2(float2 *p, float2 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(p), "f"(v.x), "f"(v.y), "l"(pol) : "memory");
+}
+
 // Byte offset of (row, dim) in a tile of 128-byte rows stored with the
 // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7).
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
@@ -191,15 +205,14 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 // Items of unit u = r*Hkv + h: 1 (the block) + ceil(L_r/64) (pages); unit u
 // covers items [ustart[u], ustart[u+1]) of the line, W = ustart[U].  Chunk j
 // of unit u covers its items [j*ch, min((j+1)*ch, items)) and leaves its
-// partial in workspace slot u * slots_per_unit + j.  CTA c of C takes the chunks whose
-// first item lies in [ceil(c*W/C), ceil((c+1)*W/C)): one run of consecutive
-// chunks per unit it touches.
+// partial in workspace slot u * slots_per_unit + j.  A CTA takes the chunks
+// whose start lies in its slice of the line (build_plan says which line and
+// how many slices): one run of consecutive chunks per unit it touches.
 
 struct Plan {
     long long ustart[kMaxUnits + 1];
     int ch[kMaxUnits];
     int nch[kMaxUnits];
-    int cstart[kMaxUnits + 1];
     int lens[kMaxR];
     int nrun;
     int run_u[kMaxUnits];
@@ -210,7 +223,6 @@ struct Plan {
 };
 static_assert(sizeof(Plan) <= 1536, "plan fits its shared-memory slot");
 
-__device__ __forceinline__ long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
 
 // Chunks a unit is cut into (before the kChunkMax cap): 16, or more when
 // there are few units so that a single request still spreads over the GPU.
@@ -221,21 +233,21 @@ __host__ __device__ constexpr int chunk_splits(int units) {
 }
 
 // Chunk size and count of a unit of `items` items (the block and its
-// pages) in a call of U units: a function of the unit's own length and the
-// call's shape only, so a chunk's partial does not depend on other requests.
+// pages) in a call of U units (splits = chunk_splits(U)): a function of the
+// unit's own length and the call's shape only, so a chunk's partial does
+// not depend on other requests.
 // Finer chunks for few units, but never below the 16-way split's chunk or 4
 // items, whichever is smaller (short units keep the 16-way chunking); chunks
 // of 5 or more items take the next power of two (8, 16, 32), so the chunk
 // sizes of long units divide one another.
-__device__ __forceinline__ void unit_chunking(int items, int U, int &ch, int &nch) {
-    const int splits = chunk_splits(U);
+__device__ __forceinline__ void unit_chunking(int items, int splits, int &ch, int &nch) {
     ch = (items + splits - 1) / splits;
     const int ch16 = (items + kChunkSplits - 1) / kChunkSplits;
     const int floor_ch = ch16 < 4 ? ch16 : 4;
     ch = ch > floor_ch ? ch : floor_ch;
     if (ch > 4) ch = 1 << (32 - __clz(ch - 1));
     ch = ch < 1 ? 1 : (ch > kChunkMax ? kChunkMax : ch);
-    nch = (items + ch - 1) / ch;
+    nch = (ch & (ch - 1)) == 0 ? (items + ch - 1) >> (31 - __clz(ch)) : (items + ch - 1) / ch;
 }
 
 // A request's context length, clamped to [0, page_stride * 64] (a length
@@ -262,36 +274,35 @@ __device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool repor
     const int U = p.R * p.Hkv;
     const int u = lane;
     const int Lu = __shfl_sync(kFull, L, (u < U ? u / p.Hkv : 0));
-    int items = 0, ch = 1, nch = 0, npages = 0;
+    int items = 0, ch = 1, nch = 0;
     if (u < U) {
-        npages = (Lu + kP - 1) / kP;
-        items = 1 + npages;
-        unit_chunking(items, U, ch, nch);
+        items = 1 + (Lu + kP - 1) / kP;
+        unit_chunking(items, p.splits, ch, nch);
     }
-    long long si = items;  // inclusive scans over units
-    int sn = nch;
+    // Inclusive scans over units of the items and of the nominal line
+    // (nch * ch); 32-bit throughout: items <= 2^25, so W, WN < 2^31.
+    const int wn = u < U ? nch * ch : 0;
+    int si = items, sw = wn, chmax = u < U ? ch : 1;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        const long long ti = __shfl_up_sync(kFull, si, off);
-        const int tn = __shfl_up_sync(kFull, sn, off);
-        if (lane >= off) { si += ti; sn += tn; }
+        const int ti = __shfl_up_sync(kFull, si, off);
+        const int tw = __shfl_up_sync(kFull, sw, off);
+        if (lane >= off) { si += ti; sw += tw; }
+        chmax = max(chmax, __shfl_xor_sync(kFull, chmax, off == 1 ? 16 : off >> 1));
     }
-    const long long base = si - items;
+    const int base = si - items;
     if (u < U) {
         pl->ustart[u] = base;
         pl->ch[u] = ch;
         pl->nch[u] = nch;
-        pl->cstart[u] = sn - nch;
     }
-    const long long W = __shfl_sync(kFull, si, U - 1);
-    const int NC = __shfl_sync(kFull, sn, U - 1);
+    const int W = __shfl_sync(kFull, si, U - 1);
+    const int WN = __shfl_sync(kFull, sw, U - 1);
     if (lane == 0) {
         pl->ustart[U] = W;
-        pl->cstart[U] = NC;
         pl->run_pq[0] = 0;
         pl->nrun = 0;
     }
-    if (cta < 0) return;
     // Which CTA computes which chunk.  With few items per CTA (W < 2 C
     // chmax, chmax the largest chunk), CTA c takes the chunks whose first
     // item lies in the c-th of C equal slices of the item line.  With many
@@ -304,41 +315,34 @@ __device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool repor
     // so the slices hold whole chunks) and all stream to the end together;
     // CTAs c >= Ce take no work.  Either way a function of the lengths that
     // only decides which CTA computes a chunk, never a chunk's boundaries.
-    int chmax = u < U ? ch : 1;
-    long long sw = u < U ? static_cast<long long>(nch) * ch : 0;  // nominal line, inclusive scan
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) chmax = max(chmax, __shfl_xor_sync(kFull, chmax, off));
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const long long t = __shfl_up_sync(kFull, sw, off);
-        if (lane >= off) sw += t;
-    }
-    const long long WN = __shfl_sync(kFull, sw, U - 1);
-    long long Ce = C, line_base = base, line_total = W;
-    if (W >= 2LL * C * chmax) {
-        const long long k = ceil_div_ll(WN, static_cast<long long>(C) * chmax);
-        Ce = ceil_div_ll(WN, k * chmax);
-        line_base = sw - (u < U ? static_cast<long long>(nch) * ch : 0);
+    int Ce = C, line_base = base, line_total = W;
+    if (W >= 2 * C * chmax) {
+        const int k = (WN + C * chmax - 1) / (C * chmax);
+        Ce = (WN + k * chmax - 1) / (k * chmax);
+        line_base = sw - wn;
         line_total = WN;
     }
-    const long long lo = ceil_div_ll(static_cast<long long>(cta) * line_total, Ce);
-    const long long hi = ceil_div_ll(static_cast<long long>(cta + 1) * line_total, Ce);
     bool has = false;
     int j0 = 0, j1 = 0, p0 = 0, npg = 0;
     if (u < U && cta < Ce) {
-        long long a = lo - line_base <= 0 ? 0 : ceil_div_ll(lo - line_base, ch);
-        long long b = hi - line_base <= 0 ? 0 : ceil_div_ll(hi - line_base, ch);
+        // Slice [ceil(c T / Ce), ceil((c + 1) T / Ce)) of the line, T =
+        // line_total, as c q + ceil(c r / Ce) with T = q Ce + r (c <= Ce,
+        // so c q <= T: no 64-bit arithmetic).
+        const int q = line_total / Ce, rem = line_total - q * Ce;
+        const int lo = cta * q + (cta * rem + Ce - 1) / Ce;
+        const int hi = (cta + 1) * q + ((cta + 1) * rem + Ce - 1) / Ce;
+        int a = lo - line_base <= 0 ? 0 : (lo - line_base + ch - 1) / ch;
+        int b = hi - line_base <= 0 ? 0 : (hi - line_base + ch - 1) / ch;
         a = a > nch ? nch : a;
         b = b > nch ? nch : b;
         if (a < b) {
             has = true;
-            j0 = static_cast<int>(a);
-            j1 = static_cast<int>(b);
+            j0 = a;
+            j1 = b;
             const int i0 = j0 * ch;
             const int i1 = j1 * ch < items ? j1 * ch : items;
             p0 = i0 == 0 ? 0 : i0 - 1;
-            const int pe = i1 - 1;
-            npg = pe - p0;
+            npg = (i1 - 1) - p0;
         }
     }
     const unsigned mask = __ballot_sync(kFull, has);
@@ -418,7 +422,8 @@ constexpr int kOffBlkV = kOffBlkK + kBlkRows * 128;  // kBlkRows rows x 128 B
 constexpr int kOffRaw = kOffBlkV + kBlkRows * 128;   // raw q [8][6][64], k [8][64], v [8][64]
 constexpr int kOffTrig = kOffRaw + kMaxB * (kG + 2) * kD * 2;  // [8][32] float2
 constexpr int kOffNormW = kOffTrig + kMaxB * 32 * 8;  // q and k norm weights, [2][64] bf16
-constexpr int kOffPlan = kOffNormW + 2 * kD * 2;
+constexpr int kOffPos = kOffNormW + 2 * kD * 2;      // positions of the call's tokens, [64] int64
+constexpr int kOffPlan = kOffPos + kMaxR * kMaxB * 8;
 constexpr int kNumBars = 2 * kStages + 8;  // full, empty, s_full[2], p_full[2], o_done[2], q_ready, done
 constexpr int kOffBar = kOffPlan + (static_cast<int>(sizeof(Plan)) + 15) / 16 * 16;
 constexpr int kOffTaddr = kOffBar + kNumBars * 8;
@@ -525,6 +530,29 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     const uint32_t bar_odone = bar_pfull + 16, bar_qready = bar_odone + 16, bar_done = bar_qready + 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // The norm weights and the positions of all the call's tokens do not
+    // depend on the plan: their loads are issued first and land while the
+    // plan is built (they go to shared memory once the row warps start).
+    __nv_bfloat16 w_early = __float2bfloat16_rn(0.f);
+    long long pos_early = 0;
+    // A row thread's RoPE pair is j = its lane (every angle it forms): its
+    // turn rate, read with constant indices (a lane-dependent index into the
+    // kernel parameters would serialize the warp's reads) and early (the
+    // first touch of a launch's parameters misses their cache).
+    // Only row warps 1-3 form angles, so warp 0 (which builds the plan)
+    // never waits for these reads.
+    unsigned long long my_rate = 0;
+    if (QKNORM && threadIdx.x < kRowThreads) {
+        w_early = threadIdx.x < kD ? p.q_w[threadIdx.x] : p.k_w[threadIdx.x - kD];
+        if (threadIdx.x < p.R * p.B)
+            pos_early = p.pos_i64 ? reinterpret_cast<const long long *>(p.positions)[threadIdx.x]
+                                  : reinterpret_cast<const int *>(p.positions)[threadIdx.x];
+        if (warp != 0) {
+#pragma unroll
+            for (int j = 0; j < kD / 2; ++j)
+                if (lane == j) my_rate = p.turn_rate[j];
+        }
+    }
     build_plan(p, pl, blockIdx.x, p.grid, blockIdx.x == 0);
     {
         // Q and block tiles start as zeros: rows without a query row or a
@@ -722,19 +750,12 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         float2 *trig = reinterpret_cast<float2 *>(smem + kOffTrig);
         const long long row_w = static_cast<long long>(p.Hq + 2 * p.Hkv) * kD;
         __nv_bfloat16 *normw = reinterpret_cast<__nv_bfloat16 *>(smem + kOffNormW);  // [0..63] q, [64..127] k
-        if (QKNORM && t < 2 * kD) normw[t] = t < kD ? p.q_w[t] : p.k_w[t - kD];
-        {
-            // Rows sit in TMEM lanes 0-11 of each quarter and P is written
-            // below for lanes 0-15 only: zero the P columns of the whole
-            // quarter once so the P.V products of the unused lanes read zeros.
-            uint32_t zero[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) zero[j] = 0u;
-#pragma unroll
-            for (uint32_t c = 0; c < 2u * kPCols; c += 32u) tmem_st32(tmem + lane_off + kColP + c, zero);
-            tmem_wait_st();
-            fence_before();
+        long long *pos_s = reinterpret_cast<long long *>(smem + kOffPos);            // [R*B]
+        if (QKNORM) {
+            normw[t] = w_early;
+            if (t < p.R * p.B) pos_s[t] = pos_early;
         }
+
         // A chunk's partial is written while the next chunk's first item is in
         // flight (its P.V, the last O reader, was confirmed just before), so
         // the wait for the chunk's last P.V hides behind that item's softmax.
@@ -750,15 +771,20 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
             if (active) {
                 // The partial's O leaves as bf16: half the bytes for the
                 // split pass to write and the combine to read; one rounding
-                // (2^-9 relative) of values the combine then averages.
+                // (2^-9 relative) of values the combine then averages.  The
+                // stores ask L2 to keep the partials (evict_last).
+                uint64_t keep;
+                asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
                 uint4 *dst = reinterpret_cast<uint4 *>(p.ws_o + epi_slot * kPartialElems + rho * kD + 32 * half);
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    dst[j] = make_uint4(pack_bf16(__uint_as_float(orr[8 * j]), __uint_as_float(orr[8 * j + 1])),
-                                        pack_bf16(__uint_as_float(orr[8 * j + 2]), __uint_as_float(orr[8 * j + 3])),
-                                        pack_bf16(__uint_as_float(orr[8 * j + 4]), __uint_as_float(orr[8 * j + 5])),
-                                        pack_bf16(__uint_as_float(orr[8 * j + 6]), __uint_as_float(orr[8 * j + 7])));
-                if (half == 0) p.ws_ml[epi_slot * kRows + rho] = make_float2(epi_m, ltot);
+                    st_hint_v4(dst + j,
+                               make_uint4(pack_bf16(__uint_as_float(orr[8 * j]), __uint_as_float(orr[8 * j + 1])),
+                                          pack_bf16(__uint_as_float(orr[8 * j + 2]), __uint_as_float(orr[8 * j + 3])),
+                                          pack_bf16(__uint_as_float(orr[8 * j + 4]), __uint_as_float(orr[8 * j + 5])),
+                                          pack_bf16(__uint_as_float(orr[8 * j + 6]), __uint_as_float(orr[8 * j + 7]))),
+                               keep);
+                if (half == 0) st_hint_f2(p.ws_ml + epi_slot * kRows + rho, make_float2(epi_m, ltot), keep);
             }
             epi_pending = false;
         };
@@ -788,30 +814,38 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                                qkv_rows + ti * row_w * 2 + head * 128 + (c & 7) * 16);
                 }
             }
-            if (QKNORM) {
-                long long pos[2] = {0, 0};
+            if (QKNORM && warp != 0) {
+                // Row warps 1-3 form the B x 32 (token, pair) angles, three
+                // each: entry e = (t - 32) + 96 k has pair e % 32 = lane.
 #pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    const int e = t + k2 * kRowThreads;
+                for (int k3 = 0; k3 < 3; ++k3) {
+                    const int e = (t - 32) + 96 * k3;
                     if (e < p.B * 32) {
-                        const long long tok = static_cast<long long>(r) * p.B + (e >> 5);
-                        pos[k2] = p.pos_i64 ? reinterpret_cast<const long long *>(p.positions)[tok]
-                                            : reinterpret_cast<const int *>(p.positions)[tok];
-                    }
-                }
-#pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    const int e = t + k2 * kRowThreads;
-                    if (e < p.B * 32) {
-                        const double theta = static_cast<double>(pos[k2]) * p.inv_freq[e & 31];
-                        const double turns = rint(theta * 0.15915494309189535);
-                        double red = fma(-turns, 6.283185307179586, theta);
-                        red = fma(-turns, 2.4492935982947064e-16, red);
+                        // The angle's fraction of a turn, exactly (integer
+                        // arithmetic wraps whole turns away); its top 32
+                        // bits are the signed fraction in [-1/2, 1/2).
+                        const unsigned long long turns =
+                            static_cast<unsigned long long>(pos_s[r * p.B + (e >> 5)]) * my_rate;
+                        const float half_turns = static_cast<float>(static_cast<int>(turns >> 32)) * 0x1p-31f;
                         float sn, cs;
-                        sincosf(static_cast<float>(red), &sn, &cs);
+                        sincospif(half_turns, &sn, &cs);
                         trig[e] = make_float2(cs * p.rope_mscale, sn * p.rope_mscale);
                     }
                 }
+            }
+            if (rn == 0) {
+                // Rows sit in TMEM lanes 0-11 of each quarter and P is
+                // written below for lanes 0-15 only: zero the P columns of
+                // the whole quarter once (while the rows above are in
+                // flight) so the P.V products of the unused lanes read zeros.
+                uint32_t zero[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) zero[j] = 0u;
+                fence_after();
+#pragma unroll
+                for (uint32_t c = 0; c < 2u * kPCols; c += 32u) tmem_st32(tmem + lane_off + kColP + c, zero);
+                tmem_wait_st();
+                fence_before();
             }
             cp_async_wait_all();
             if (it > 0) {
@@ -1038,8 +1072,9 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
 // One CTA per (unit, 2 query rows), 128 threads: thread = (row, 8 dims,
 // chunk lane sg of 8), the 8 chunk lanes of one (row, dims) adjacent in a
 // warp.  Lane sg folds the unit's chunk partials sg, sg+8, ... online; it
-// issues the loads of up to kCombineFold of them at once, so a unit of up to
-// 72 chunks is read in one round trip; the lanes then merge by a fixed
+// issues the loads of kCombineFold of them at once (deeper folds measured
+// slower on the 8x8 workloads and no faster on long contexts); the lanes
+// then merge by a fixed
 // butterfly of shuffles, so the result depends on nothing but the unit's own
 // chunks.  Launched as a programmatic dependent of the split pass: the
 // unit's chunk count comes from its context length (an input, read before
@@ -1048,7 +1083,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
 // the split pass.
 constexpr int kCombineRows = 2;
 constexpr int kCombineLanes = 8;
-constexpr int kCombineFold = 9;
+constexpr int kCombineFold = 4;
 
 __global__ void __launch_bounds__(128, 6) k3da_combine_kernel(const __grid_constant__ Params p) {
     const int per_unit = kRows / kCombineRows;
@@ -1061,7 +1096,7 @@ __global__ void __launch_bounds__(128, 6) k3da_combine_kernel(const __grid_const
     bool bad;
     const int L = clamped_length(p, __ldg(p.ctx_lens + r), &bad);
     int ch, nch;
-    unit_chunking(1 + (L + kP - 1) / kP, p.R * p.Hkv, ch, nch);
+    unit_chunking(1 + (L + kP - 1) / kP, p.splits, ch, nch);
     const uint8_t *slots = reinterpret_cast<const uint8_t *>(p.ws_o) +
                            static_cast<long long>(u) * p.slots_per_unit * kPartialElems * 2;
     const float2 *mls = p.ws_ml + static_cast<long long>(u) * p.slots_per_unit * kRows;
@@ -1393,6 +1428,7 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
     prm.k_w = static_cast<const __nv_bfloat16 *>(k_norm_w);
     const size_t slots = workspace_slots(R, Hkv, page_stride);
     prm.slots_per_unit = static_cast<int>(slots_per_unit(R, Hkv, page_stride));
+    prm.splits = chunk_splits(R * Hkv);
     prm.ws_o = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(workspace) + kWsHeaderBytes);
     prm.ws_ml = reinterpret_cast<float2 *>(prm.ws_o + slots * kPartialElems);
     prm.status = status;
@@ -1407,7 +1443,11 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
     prm.grid = cfg.sms * occ;
     prm.scale_log2 = softmax_scale * 1.4426950408889634f;
     prm.eps = eps;
-    k3da_host::rope_frequencies(prm.inv_freq, kD / 2, rope_base, yarn);
+    {
+        double inv_freq[kD / 2];
+        k3da_host::rope_frequencies(inv_freq, kD / 2, rope_base, yarn);
+        for (int j = 0; j < kD / 2; ++j) prm.turn_rate[j] = k3da_host::turn_rate_fixed64(inv_freq[j]);
+    }
     prm.rope_mscale = yarn != nullptr ? k3da_host::yarn_mscale(yarn) : 1.0f;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);

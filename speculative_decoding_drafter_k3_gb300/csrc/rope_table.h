@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cmath>
+#include <cstdint>
 
 #include "k3da.h"
 
@@ -44,6 +45,32 @@ inline void rope_frequencies(double *inv_freq, int pairs, float base, const k3da
         ramp = ramp < 0.0 ? 0.0 : (ramp > 1.0 ? 1.0 : ramp);
         inv_freq[j] = theta * ramp + theta / static_cast<double>(yarn->factor) * (1.0 - ramp);
     }
+}
+
+// A rotary frequency f (radians per position, 0 < f <= 1) as a turn rate:
+// round(f * 2^64 / (2 pi)), unsigned 64-bit fixed point with 2^64 = one
+// turn.  For an integer position p, p * turn_rate mod 2^64 (plain wrapping
+// integer arithmetic) is then p f / (2 pi) mod 1, the angle's fraction of a
+// turn, exact up to p * 2^-65 turns: no floating-point range reduction.
+// Formed exactly from the fp64 f with 128-bit integer arithmetic and
+// floor(2^128 / (2 pi)) = kInv2PiHi * 2^64 + kInv2PiLo.
+inline uint64_t turn_rate_fixed64(double f) {
+    constexpr uint64_t kInv2PiHi = 0x28BE60DB9391054Aull;
+    constexpr uint64_t kInv2PiLo = 0x7F09D5F47D4D3770ull;
+    if (!(f > 0.0) || !(f <= 1.0)) return 0;
+    int ex = 0;
+    const double fr = std::frexp(f, &ex);  // f = fr * 2^ex, fr in [0.5, 1)
+    const uint64_t m = static_cast<uint64_t>(std::ldexp(fr, 53));  // exact: f = m * 2^(ex - 53)
+    // f * 2^64 / (2 pi) = m * K * 2^(ex - 53 - 128 + 64) with K = 2^128 / (2 pi):
+    // the product m * K (up to 179 bits) is high * 2^64 + low, shifted right
+    // by rs = 117 - ex bits (>= 116 since ex <= 1).
+    const unsigned __int128 p1 = static_cast<unsigned __int128>(m) * kInv2PiHi;
+    const unsigned __int128 p0 = static_cast<unsigned __int128>(m) * kInv2PiLo;
+    const unsigned __int128 high = p1 + (p0 >> 64);
+    const int rs = 117 - ex - 64;  // shift of `high`
+    if (rs >= 127) return 0;
+    const unsigned __int128 half = static_cast<unsigned __int128>(1) << (rs - 1);
+    return static_cast<uint64_t>((high + half) >> rs);
 }
 
 }  // namespace k3da_host

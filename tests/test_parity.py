@@ -3,6 +3,8 @@ five workloads of the drafter block attention (6/1 and 24/4 heads, every
 request x token split, context lengths 0..2041 and 16k..128k, dense and
 strided page-table rows, int32 and int64 positions), plus edge cases.
 Tolerance: |gpu - oracle| <= 2e-2 + 2e-2 |oracle| on the bf16 output."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -125,3 +127,57 @@ def test_long_context_every_request():
     ref = ou.oracle_call(case)
     assert not np.isnan(ref).any()
     assert_close(out, ref, "long_context")
+
+
+BALANCED_LENS = [131072, 2041, 0, 64, 65536, 16385, 1, 100000]
+
+
+def _balanced_pair():
+    """Two calls that differ only in request 2's context (0 tokens, then
+    5000): same pool, qkv, norm weights and page-table rows (each a slice of
+    one page permutation, sized for the longer of the two lengths; entries
+    past a context are never read)."""
+    lens1 = list(BALANCED_LENS)
+    lens2 = list(BALANCED_LENS)
+    lens2[2] = 5000
+    need = [(max(a, b) + 63) // 64 for a, b in zip(lens1, lens2)]
+    g = torch.Generator().manual_seed(66)
+    perm = torch.randperm(sum(need) + 16, generator=g).to(torch.int32)
+    case = workloads.build_case("balanced_mixed", R=8, B=8, Hq=24, Hkv=4, lens=[0] * 8, page_stride=2048,
+                                num_pages=sum(need) + 16, used_per_row=1, qknorm=True,
+                                pos_dtype=torch.int64, seed=66, device="cuda")
+    pt = torch.full((8, 2048), -1, dtype=torch.int32)
+    off = 0
+    for r, n in enumerate(need):
+        pt[r, :n] = perm[off:off + n]
+        off += n
+    case.page_table.copy_(pt)
+    cases = []
+    for lens in (lens1, lens2):
+        c = dataclasses.replace(case, ctx_lens=torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                                positions=torch.tensor([L + i for L in lens for i in range(8)],
+                                                       dtype=torch.int64, device="cuda"))
+        cases.append(c)
+    return cases
+
+
+def test_balanced_assignment_with_mixed_chunk_sizes():
+    """Contexts long enough for the balanced assignment (every CTA holds
+    several 32-page chunks, so the work is cut on the nominal line of chunk
+    sizes) mixed with short ones (3- and 1-item chunks): every request
+    matches the oracle, and changing one request's length, which moves
+    every CTA's share of the work, leaves the other requests' rows bitwise
+    unchanged."""
+    case1, case2 = _balanced_pair()
+    out1, st1 = run(case1)
+    out1 = out1.clone()
+    assert st1 == 0
+    assert_close(out1, ou.oracle_call(case1), "balanced_mixed")
+    out2, st2 = run(case2)
+    assert st2 == 0
+    for r in range(8):
+        if r != 2:
+            sl = slice(r * 8, (r + 1) * 8)
+            assert torch.equal(out1[sl].view(torch.int16), out2[sl].view(torch.int16)), r
+    ref2 = ou.oracle_call(case2, requests=[2])
+    assert_close(out2[16:24], ref2[16:24], "balanced_mixed r2")

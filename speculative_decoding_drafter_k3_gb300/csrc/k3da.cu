@@ -385,12 +385,13 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // shapes whatever N, so two issuers double the tensor throughput of a CTA):
 //   S[b] (128 x 64 fp32, TMEM)  = Q (128 x 64, smem) . K_page^T
 //   O    (128 x 64 fp32, TMEM) += P[b] (bf16, TMEM) . V_page
-// with two S buffers so the next item's QK^T overlaps this item's softmax.
-// The softmax keeps a per-row exponent base m; P = 2^(s*scale*log2e - m) is
-// written as bf16 to TMEM buffer P[b] (each thread its half of the row's
-// keys; kept apart from S[b] so that the next QK^T into S[b] never
-// overwrites a P the previous PV may still be reading) and becomes the A
-// operand of the PV MMA, which leaves the row's whole O in its lane.  O is
+// with three buffers b = item mod 3.  The softmax keeps a per-row exponent
+// base m; P = 2^(s*scale*log2e - m) is written as bf16 over the first half
+// of the item's own S buffer once the warp has read it (each thread its half
+// of the row's keys) and becomes the A operand of the PV MMA, which leaves
+// the row's whole O in its lane.  The QK^T of item i+3 reuses the buffer
+// once item i's PV has read its P, so the softmax never waits for a PV to
+// free a P buffer, and QK^T runs up to two items ahead of it.  O is
 // only rescaled when a row's maximum passes m by more than 8 (log2 units;
 // P <= 256 is exact enough in bf16 and fp32), so the common path never
 // touches O.
@@ -403,14 +404,13 @@ constexpr int kProducerWarp = kRowWarps;
 constexpr int kQkWarp = kRowWarps + 1;  // issues the QK^T products (and owns the TMEM allocation)
 constexpr int kPvWarp = kRowWarps + 2;  // issues the P.V products
 constexpr int kThreads = 32 * (kRowWarps + 3);
-// Tensor memory: S[b] (64 columns) at 64*b, O at 128, then P[b] (32
-// columns of bf16 pairs) at kColP + 32*b.
+// Tensor memory: S/P buffer b (64 columns; P, 32 columns of bf16 pairs,
+// over its first half) at 64*b, O at 192.
+constexpr uint32_t kSBufs = 3;
 constexpr uint32_t kSCols = 64u;
-constexpr uint32_t kColO = 2u * kSCols;
-constexpr uint32_t kColP = kColO + 64u;
-constexpr uint32_t kPCols = 32u;
+constexpr uint32_t kColO = kSBufs * kSCols;
 constexpr uint32_t kTmemCols = 256u;
-static_assert(kColP + 2u * kPCols <= kTmemCols, "tensor memory columns");
+static_assert(kColO + 64u <= kTmemCols, "tensor memory columns");
 constexpr int kCtasPerSm = 2;  // 2 x 256 of the SM's 512 TMEM columns
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // Shared memory (offsets from a 1024-byte aligned base).
@@ -424,7 +424,7 @@ constexpr int kOffTrig = kOffRaw + kMaxB * (kG + 2) * kD * 2;  // [8][32] float2
 constexpr int kOffNormW = kOffTrig + kMaxB * 32 * 8;  // q and k norm weights, [2][64] bf16
 constexpr int kOffPos = kOffNormW + 2 * kD * 2;      // positions of the call's tokens, [64] int64
 constexpr int kOffPlan = kOffPos + kMaxR * kMaxB * 8;
-constexpr int kNumBars = 2 * kStages + 8;  // full, empty, s_full[2], p_full[2], o_done[2], q_ready, done
+constexpr int kNumBars = 2 * kStages + 3 * kSBufs + 2;  // full, empty, s_full[3], p_full[3], o_done[3], q_ready, done
 constexpr int kOffBar = kOffPlan + (static_cast<int>(sizeof(Plan)) + 15) / 16 * 16;
 constexpr int kOffTaddr = kOffBar + kNumBars * 8;
 constexpr int kOffFlag = kOffTaddr + 8;
@@ -483,12 +483,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 consecutive 32-bit TMEM columns of each lane of the warp's quarter.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-                 : "memory");
-}
-
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Half-split access (shape 16x32bx2): threads 0-15 reach TMEM lanes
@@ -526,8 +520,8 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     uint32_t *taddr_slot = reinterpret_cast<uint32_t *>(smem + kOffTaddr);
     const uint32_t bars = smem_u32(smem + kOffBar);
     const uint32_t bar_full = bars, bar_empty = bars + 8 * kStages;
-    const uint32_t bar_sfull = bars + 16 * kStages, bar_pfull = bar_sfull + 16;
-    const uint32_t bar_odone = bar_pfull + 16, bar_qready = bar_odone + 16, bar_done = bar_qready + 8;
+    const uint32_t bar_sfull = bars + 16 * kStages, bar_pfull = bar_sfull + 8 * kSBufs;
+    const uint32_t bar_odone = bar_pfull + 8 * kSBufs, bar_qready = bar_odone + 8 * kSBufs, bar_done = bar_qready + 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // The norm weights and the positions of all the call's tokens do not
@@ -567,12 +561,11 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
-        mbar_init(bar_sfull, 1);
-        mbar_init(bar_sfull + 8, 1);
-        mbar_init(bar_pfull, kRowWarps);
-        mbar_init(bar_pfull + 8, kRowWarps);
-        mbar_init(bar_odone, 1);
-        mbar_init(bar_odone + 8, 1);
+        for (int b = 0; b < static_cast<int>(kSBufs); ++b) {
+            mbar_init(bar_sfull + 8 * b, 1);
+            mbar_init(bar_pfull + 8 * b, kRowWarps);
+            mbar_init(bar_odone + 8 * b, 1);
+        }
         mbar_init(bar_qready, kRowWarps);
         mbar_init(bar_done, 2);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -675,14 +668,14 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                 const int i0 = jc * ch;
                 const int i1 = i0 + ch < items ? i0 + ch : items;
                 for (int item = i0; item < i1; ++item, ++it) {
-                    const int b = static_cast<int>(it & 1);
+                    const int b = static_cast<int>(static_cast<uint32_t>(it) % kSBufs);
+                    const uint32_t ph = (static_cast<uint32_t>(it) / kSBufs) & 1u;
                     const bool is_page = item > 0;
                     const int s = static_cast<int>(kr % kStages);
                     if (is_page) ++kr;
                     if (is_qk) {
-                        if (it >= 2) {  // S[b] is free once item it-2's P is out
-                            mbar_wait(bar_pfull + 8 * b, static_cast<uint32_t>(((it - 2) >> 1) & 1), abort_flag,
-                                      p.status);
+                        if (it >= kSBufs) {  // buffer b is free once item it-3's P.V has read its P
+                            mbar_wait(bar_odone + 8 * b, ph ^ 1u, abort_flag, p.status);
                             fence_after();
                         }
                         if (is_page) {
@@ -703,10 +696,10 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                         __syncwarp();
                     } else {
                         const bool first = item == i0;
-                        mbar_wait(bar_pfull + 8 * b, static_cast<uint32_t>((it >> 1) & 1), abort_flag, p.status);
+                        mbar_wait(bar_pfull + 8 * b, ph, abort_flag, p.status);
                         fence_after();
                         if (lane == 0) {
-                            const uint32_t pcol = tmem + kColP + kPCols * b;
+                            const uint32_t pcol = tmem + kSCols * b;
                             if (!is_page) {
                                 // The block: at most 8 keys, all in the first 16-key step.
                                 mma_ts(tmem + kColO, pcol, bv_desc, kIdescPV, first ? 0u : 1u);
@@ -718,7 +711,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                                     mma_ts(tmem + kColO, pcol + 8u * kk, v_desc + ((kk * 2048) >> 4), kIdescPV,
                                            (kk > 0 || !first) ? 1u : 0u);
                             }
-                            mma_commit(bar_odone + 8 * b);  // o_done[it & 1]
+                            mma_commit(bar_odone + 8 * b);  // o_done[it % 3]
                             if (is_page) mma_commit(bar_empty + 8 * s);
                         }
                         __syncwarp();
@@ -833,26 +826,12 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                     }
                 }
             }
-            if (rn == 0) {
-                // Rows sit in TMEM lanes 0-11 of each quarter and P is
-                // written below for lanes 0-15 only: zero the P columns of
-                // the whole quarter once (while the rows above are in
-                // flight) so the P.V products of the unused lanes read zeros.
-                uint32_t zero[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) zero[j] = 0u;
-                fence_after();
-#pragma unroll
-                for (uint32_t c = 0; c < 2u * kPCols; c += 32u) tmem_st32(tmem + lane_off + kColP + c, zero);
-                tmem_wait_st();
-                fence_before();
-            }
             cp_async_wait_all();
             if (it > 0) {
                 // The block tiles are rewritten below: the last P.V (which
                 // may have read the previous block's V) must be complete.
-                mbar_wait(bar_odone + 8 * static_cast<uint32_t>((it - 1) & 1),
-                          static_cast<uint32_t>(((it - 1) >> 1) & 1), abort_flag, p.status);
+                mbar_wait(bar_odone + 8 * (static_cast<uint32_t>(it - 1) % kSBufs),
+                          (static_cast<uint32_t>(it - 1) / kSBufs) & 1u, abort_flag, p.status);
                 fence_after();
             }
             named_bar_sync(1, kRowThreads);
@@ -951,7 +930,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                 const int i0 = jc * ch;
                 const int i1 = i0 + ch < items ? i0 + ch : items;
                 for (int item = i0; item < i1; ++item) {
-                    const int b = static_cast<int>(it & 1);
+                    const int b = static_cast<int>(static_cast<uint32_t>(it) % kSBufs);
                     const bool is_page = item > 0;
                     const int s = static_cast<int>(kr % kStages);
                     int valid = p.B;
@@ -959,7 +938,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                         const int left = L - (item - 1) * kP;
                         valid = left < kP ? left : kP;
                     }
-                    mbar_wait(bar_sfull + 8 * b, static_cast<uint32_t>((it >> 1) & 1), abort_flag, p.status);
+                    mbar_wait(bar_sfull + 8 * b, (static_cast<uint32_t>(it) / kSBufs) & 1u, abort_flag, p.status);
                     fence_after();
                     // This thread's half of the page's keys.
                     float sv[32];
@@ -998,23 +977,23 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                             pk[j] = pack_bf16(p0, p1);
                         }
                         // The row's P: this thread's half of the keys, 16
-                        // columns of bf16 pairs.
-                        tmem_st_h16(tmem + lane_off + kColP + kPCols * b, pk);
+                        // columns of bf16 pairs, over the S just read.
+                        tmem_st_h16(tmem + lane_off + kSCols * b, pk);
                     }
                     lsum = (first ? 0.f : lsum * f) + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
                     m_used = m_new;
                     tmem_wait_st();
                     // O is touched (a chunk's partial, a rescale) only once the
                     // previous item's P.V is complete; otherwise P is handed
-                    // over at once and that P.V is confirmed after the
-                    // hand-over.  Item i's P.V completes phase i/2 of
-                    // o_done[i & 1], whose next phase needs item i+2's P, so
-                    // the confirmation cannot be overtaken.
+                    // over at once.  Item i's P.V completes phase i/3 of
+                    // o_done[i % 3]; its next phase needs item i+3's P, and
+                    // the one before (item i-3's P.V) completed before item
+                    // i's QK^T could start, so a wait on it is never a phase
+                    // off.
                     const bool touch_o = epi_pending || __any_sync(kFull, need);
-                    const uint32_t od_bar = bar_odone + 8 * static_cast<uint32_t>((it - 1) & 1);
-                    const uint32_t od_par = static_cast<uint32_t>(((it - 1) >> 1) & 1);
                     if (touch_o && it > 0) {
-                        mbar_wait(od_bar, od_par, abort_flag, p.status);
+                        mbar_wait(bar_odone + 8 * (static_cast<uint32_t>(it - 1) % kSBufs),
+                                  (static_cast<uint32_t>(it - 1) / kSBufs) & 1u, abort_flag, p.status);
                         fence_after();
                     }
                     if (epi_pending) write_partial();  // before this item's P.V overwrites O
@@ -1039,7 +1018,6 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                     fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_pfull + 8 * b);
-                    if (!touch_o && it > 0) mbar_wait(od_bar, od_par, abort_flag, p.status);
                     ++it;
                     if (is_page) ++kr;
                 }
@@ -1051,8 +1029,8 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
             }
         }
         if (epi_pending) {
-            mbar_wait(bar_odone + 8 * static_cast<uint32_t>((it - 1) & 1), static_cast<uint32_t>(((it - 1) >> 1) & 1),
-                      abort_flag, p.status);
+            mbar_wait(bar_odone + 8 * (static_cast<uint32_t>(it - 1) % kSBufs),
+                      (static_cast<uint32_t>(it - 1) / kSBufs) & 1u, abort_flag, p.status);
             fence_after();
             write_partial();
         }

@@ -390,8 +390,9 @@ MUTANTS = {
     # the wait for S of an item, then its TMEM load
     "no_fence_after_s_full_wait": ("mbar_wait(bar_sfull + 8 * b", "fence_after();", True, "A"),
     # the wait for P of an item, then the P.V MMA
-    "no_fence_after_p_full_wait": ("mbar_wait(bar_pfull + 8 * b, static_cast<uint32_t>((it >> 1) & 1)",
-                                   "fence_after();", True, "A"),
+    "no_fence_after_p_full_wait": ("mbar_wait(bar_pfull + 8 * b, ph", "fence_after();", True, "A"),
+    # the P.V that freed an S/P buffer, then the next QK^T into it
+    "no_fence_after_buffer_free_wait": ("mbar_wait(bar_odone + 8 * b, ph ^ 1u", "fence_after();", True, "A"),
     # the page's TMA data, then the QK^T MMA
     "no_fence_after_page_wait": ("mbar_wait(bar_full + 8 * s, static_cast<uint32_t>(((kr - 1) / kStages) & 1)",
                                  "fence_after();", True, "A"),

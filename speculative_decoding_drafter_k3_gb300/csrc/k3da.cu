@@ -375,16 +375,17 @@ __device__ __forceinline__ void cp_async_wait_all() {
 //
 // The two contractions run on the 5th-generation tensor cores.  An item is
 // the block or one page.  Row warp w owns TMEM lane quarter q = w: query row
-// rho = 12*q + l (l < 12) is Q-tile row (and TMEM lane) 32*q + l.  Threads
+// rho = 12*q + l (l < 12) is Q-tile row 16*q + l and TMEM lane 32*q + l (the
+// M = 64 MMAs put rows 16q..16q+15 in lanes 0-15 of lane quarter q).  Threads
 // l and l + 16 of the warp share that lane through the half-split TMEM
 // access (shape 16x32bx2): the first handles keys 0..31 of its page, the
 // second keys 32..63, so a row's softmax costs two threads half a page each
 // and one shuffle to share the row maximum.  The producer warp streams K/V
 // pages with TMA; one warp issues the QK^T products and another the P.V
-// products (a thread issues one MMA at a time, ~156 cycles each at these
-// shapes whatever N, so two issuers double the tensor throughput of a CTA):
-//   S[b] (128 x 64 fp32, TMEM)  = Q (128 x 64, smem) . K_page^T
-//   O    (128 x 64 fp32, TMEM) += P[b] (bf16, TMEM) . V_page
+// products (a thread issues one MMA at a time, so two issuers double the
+// tensor work a CTA can have in flight):
+//   S[b] (64 x 64 fp32, TMEM)  = Q (64 x 64, smem) . K_page^T
+//   O    (64 x 64 fp32, TMEM) += P[b] (bf16, TMEM) . V_page
 // with three buffers b = item mod 3.  The softmax keeps a per-row exponent
 // base m; P = 2^(s*scale*log2e - m) is written as bf16 over the first half
 // of the item's own S buffer once the warp has read it (each thread its half
@@ -396,7 +397,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // P <= 256 is exact enough in bf16 and fp32), so the common path never
 // touches O.
 namespace tc {
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kRowWarps = 4;  // one warp per TMEM lane quarter
 constexpr int kRowThreads = 32 * kRowWarps;
 constexpr int kRowsPerQuarter = 12;
@@ -415,9 +416,10 @@ constexpr int kCtasPerSm = 2;  // 2 x 256 of the SM's 512 TMEM columns
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // Shared memory (offsets from a 1024-byte aligned base).
 constexpr int kOffStages = 0;                        // kStages x (K tile, V tile)
-constexpr int kOffQ = kStages * kStageBytes;         // 128 rows x 128 B, 128B swizzle
+constexpr int kOffQ = kStages * kStageBytes;         // kQRows rows x 128 B, 128B swizzle
 constexpr int kBlkRows = 16;                          // block tiles: B <= 8 keys, one 16-row MMA step
-constexpr int kOffBlkK = kOffQ + 128 * 128;          // kBlkRows rows x 128 B
+constexpr int kQRows = 64;                            // M of the MMAs: rows 16q..16q+15 -> TMEM lanes 32q..32q+15
+constexpr int kOffBlkK = kOffQ + kQRows * 128;        // kBlkRows rows x 128 B
 constexpr int kOffBlkV = kOffBlkK + kBlkRows * 128;  // kBlkRows rows x 128 B
 constexpr int kOffRaw = kOffBlkV + kBlkRows * 128;   // raw q [8][6][64], k [8][64], v [8][64]
 constexpr int kOffTrig = kOffRaw + kMaxB * (kG + 2) * kD * 2;  // [8][32] float2
@@ -442,9 +444,9 @@ static_assert(kOffBar % 8 == 0 && kOffPlan % 8 == 0, "mbarrier / int64 alignment
 constexpr uint32_t idesc_f16(uint32_t m, uint32_t n, bool b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? 1u << 16 : 0u) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
-constexpr uint32_t kIdescQK = idesc_f16(128, 64, false);            // a page's keys
-constexpr uint32_t kIdescQKBlock = idesc_f16(128, kBlkRows, false); // the block tile
-constexpr uint32_t kIdescPV = idesc_f16(128, 64, true);
+constexpr uint32_t kIdescQK = idesc_f16(kQRows, 64, false);            // a page's keys
+constexpr uint32_t kIdescQKBlock = idesc_f16(kQRows, kBlkRows, false); // the block tile
+constexpr uint32_t kIdescPV = idesc_f16(kQRows, 64, true);
 
 // Shared-memory matrix descriptor of a tile stored in 128-byte rows with the
 // 128-byte swizzle (8-row, 1 KB atoms): start address >> 4 (bits 0-13),
@@ -552,7 +554,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         // Q and block tiles start as zeros: rows without a query row or a
         // block token stay zero for the whole kernel.
         uint4 *z = reinterpret_cast<uint4 *>(smem + kOffQ);
-        for (int e = threadIdx.x; e < (128 * 128 + 2 * kBlkRows * 128) / 16; e += kThreads) z[e] = make_uint4(0, 0, 0, 0);
+        for (int e = threadIdx.x; e < (kQRows * 128 + 2 * kBlkRows * 128) / 16; e += kThreads) z[e] = make_uint4(0, 0, 0, 0);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (threadIdx.x == 0) {
@@ -851,7 +853,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                         ti = rix - g * p.B;
                         src = raw_q + (ti * kG + g) * 128;
                         dst = qtile;
-                        drow = (rix / kRowsPerQuarter) * 32 + rix % kRowsPerQuarter;
+                        drow = (rix / kRowsPerQuarter) * 16 + rix % kRowsPerQuarter;
                         norm = QKNORM;
                     }
                 } else if (rix < kRows + kMaxB) {

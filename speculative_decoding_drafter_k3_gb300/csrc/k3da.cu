@@ -177,6 +177,42 @@ __device__ __forceinline__ float exp2_approx(float x) {
     return y;
 }
 
+// Pairs of fp32 in one 64-bit register pair (x in the low word) for the
+// paired fp32 arithmetic of sm_100-family GPUs (f32x2: each lane rounded
+// like its scalar instruction).
+__device__ __forceinline__ unsigned long long pack_f32x2(float x, float y) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+
+__device__ __forceinline__ float2 unpack_f32x2(unsigned long long v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+
+__device__ __forceinline__ unsigned long long fma_f32x2(unsigned long long a, unsigned long long b,
+                                                        unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// max(a, b, c) in one instruction (sm_100 family); NaN operands are dropped
+// as by fmaxf.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+__device__ __forceinline__ unsigned long long add_f32x2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -959,8 +995,10 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) mx[j] = sv[j];
 #pragma unroll
-                    for (int j = 4; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], sv[j]);
-                    float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                    for (int j = 4; j < 28; j += 8)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) mx[k] = fmax3(mx[k], sv[j + k], sv[j + 4 + k]);
+                    float rmax = fmax3(fmax3(mx[0], sv[28], sv[29]), fmax3(mx[1], sv[30], sv[31]), fmax3(mx[2], mx[3], mx[3]));
                     rmax = fmaxf(rmax, __shfl_xor_sync(kFull, rmax, 16)) * p.scale_log2;
                     // Exponent base: the row max on a chunk's first item; later,
                     // only when the max passes the base by more than 2^8.
@@ -968,21 +1006,27 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                     const bool need = !first && rmax > m_used + kRescaleThreshold;
                     const float m_new = (first || need) ? rmax : m_used;
                     const float f = need ? exp2_approx(m_used - m_new) : 1.f;
-                    float rs[4] = {0.f, 0.f, 0.f, 0.f};
+                    // Keys 2j and 2j + 1 go through the paired fp32 units:
+                    // s*scale - m as one f32x2 FMA, the row sum as f32x2 adds.
+                    unsigned long long rs2[2] = {0ull, 0ull};
                     {
+                        const unsigned long long sl2 = pack_f32x2(p.scale_log2, p.scale_log2);
+                        const unsigned long long nm2 = pack_f32x2(-m_new, -m_new);
                         uint32_t pk[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const float p0 = exp2_approx(fmaf(sv[2 * j], p.scale_log2, -m_new));
-                            const float p1 = exp2_approx(fmaf(sv[2 * j + 1], p.scale_log2, -m_new));
-                            rs[j & 3] += p0 + p1;
+                            const float2 x = unpack_f32x2(fma_f32x2(pack_f32x2(sv[2 * j], sv[2 * j + 1]), sl2, nm2));
+                            const float p0 = exp2_approx(x.x);
+                            const float p1 = exp2_approx(x.y);
+                            rs2[j & 1] = add_f32x2(rs2[j & 1], pack_f32x2(p0, p1));
                             pk[j] = pack_bf16(p0, p1);
                         }
                         // The row's P: this thread's half of the keys, 16
                         // columns of bf16 pairs, over the S just read.
                         tmem_st_h16(tmem + lane_off + kSCols * b, pk);
                     }
-                    lsum = (first ? 0.f : lsum * f) + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+                    const float2 rsum = unpack_f32x2(add_f32x2(rs2[0], rs2[1]));
+                    lsum = (first ? 0.f : lsum * f) + (rsum.x + rsum.y);
                     m_used = m_new;
                     tmem_wait_st();
                     // O is touched (a chunk's partial, a rescale) only once the

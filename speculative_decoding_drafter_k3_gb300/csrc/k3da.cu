@@ -683,12 +683,12 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         }
     } else if ((warp == kQkWarp || warp == kPvWarp) && nrun > 0) {
         // ------------------------------------------------- MMA warps --
-        // A thread issues one tcgen05.mma at a time (about 156 cycles each at
-        // these shapes, whatever N), so the two products have an issuing
-        // warp each.  The QK^T warp fills S[b] for item i once the row warps
-        // have released it (item i-2 done).  The P.V warp accumulates O once
-        // item i's P is in TMEM, then releases the page's stage (the item's
-        // QK^T completed before its softmax began).
+        // A thread issues one tcgen05.mma at a time, so the two products
+        // have an issuing warp each.  The QK^T warp fills buffer b = i mod 3
+        // for item i once item i-3's P.V has read the P stored there.  The
+        // P.V warp accumulates O once item i's P is in TMEM, then releases
+        // the page's stage (the item's QK^T completed before its softmax
+        // began).
         const bool is_qk = warp == kQkWarp;
         const uint64_t q_desc = desc_sw128(smem_u32(smem + kOffQ));
         const uint64_t bk_desc = desc_sw128(smem_u32(smem + kOffBlkK));

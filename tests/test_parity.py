@@ -107,6 +107,49 @@ def test_large_positions_keep_rope_angles_exact():
     check(case)
 
 
+def _rescale_case(R, Hq, Hkv, L, seed):
+    """A plain-variant case whose row maximum jumps once per 8 pages.
+
+    Every query row is 1/8 (all dims).  The keys of pages 5, 13, 21, ... of
+    each context are 6 (all dims) and all other keys, block keys included,
+    are 0.  So those pages score 6 * 1.4427 = 8.7 log2 units above the rest,
+    more than the 8 past which the split pass moves a row's exponent base and
+    rescales its O.  Whatever power-of-two chunk size of 4 items or more a
+    unit gets, such a page sits inside a chunk whose first item scores 0, so
+    every such chunk rescales once, at a position that differs between
+    chunks (and so at every S/P buffer index).  Values are +1 on the high
+    pages and -1 elsewhere (plus 0.1 N(0, 1)).  The output is then about
+    +0.98; an O or l left unscaled moves it far from that."""
+    n = L // 64
+    case = workloads.build_case(f"rescale_{R}x8_{Hq}/{Hkv}_L{L}", R=R, B=8, Hq=Hq, Hkv=Hkv, lens=[L] * R,
+                                page_stride=n, num_pages=R * n, qknorm=False, seed=seed, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    qkv = case.qkv.view(case.T, Hq + 2 * Hkv, 64)
+    qkv[:, :Hq] = 0.125
+    qkv[:, Hq:Hq + Hkv] = 0.0
+    qkv[:, Hq + Hkv:] = (-1.0 + 0.1 * torch.randn(qkv[:, Hq + Hkv:].shape, generator=g, device="cuda")).to(torch.bfloat16)
+    high = torch.zeros(R * n, dtype=torch.bool, device="cuda")
+    pages = case.page_table[:, :n].long()
+    high[pages[:, 5::8].reshape(-1)] = True
+    pool = case.pool
+    pool[:, 0] = 0.0
+    pool[high, 0] = 6.0
+    noise = 0.1 * torch.randn(pool[:, 1].shape, generator=g, device="cuda")
+    sign = torch.where(high, 1.0, -1.0).view(-1, 1, 1, 1)
+    pool[:, 1] = (sign + noise).to(torch.bfloat16)
+    return case
+
+
+@pytest.mark.parametrize("R,Hq,Hkv,L", [(2, 6, 1, 65536), (8, 24, 4, 40960), (1, 6, 1, 8192)])
+def test_rows_whose_maximum_jumps_mid_chunk(R, Hq, Hkv, L):
+    case = _rescale_case(R, Hq, Hkv, L, seed=90 + R)
+    ref = oracle_for(case)
+    assert 0.9 < float(np.median(ref)) < 1.0  # the high pages dominate, the low ones still count
+    out, st = run(case)
+    assert st == 0
+    assert_close(out, ref, case.name)
+
+
 def test_production_block_width_w6_8x6():
     check(workloads.w6_8x6(device="cuda"))
 

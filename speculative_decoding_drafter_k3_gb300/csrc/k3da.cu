@@ -457,9 +457,17 @@ constexpr int kBlkRows = 16;                          // block tiles: B <= 8 key
 constexpr int kQRows = 64;                            // M of the MMAs: rows 16q..16q+15 -> TMEM lanes 32q..32q+15
 constexpr int kOffBlkK = kOffQ + kQRows * 128;        // kBlkRows rows x 128 B
 constexpr int kOffBlkV = kOffBlkK + kBlkRows * 128;  // kBlkRows rows x 128 B
-constexpr int kOffRaw = kOffBlkV + kBlkRows * 128;   // raw q [8][6][64], k [8][64], v [8][64]
-constexpr int kOffTrig = kOffRaw + kMaxB * (kG + 2) * kD * 2;  // [8][32] float2
-constexpr int kOffNormW = kOffTrig + kMaxB * 32 * 8;  // q and k norm weights, [2][64] bf16
+// Raw q [8][6], k [8] and v [8] rows of 128 B, each at a 144-byte stride: the
+// two threads of a row read it in 16-byte pieces, and at a 128-byte stride
+// (or the 768-byte one of a token's six q rows) the 16 rows of a warp would
+// all fall on the same four banks.
+constexpr int kRawStride = 144;
+constexpr int kOffRaw = kOffBlkV + kBlkRows * 128;
+// RoPE (cos, sin) of pair j and token i at [j][i], kMaxB + 1 entries per
+// pair: a warp's rows read one pair for up to 8 tokens at a time.
+constexpr int kTrigStride = kMaxB + 1;
+constexpr int kOffTrig = kOffRaw + kMaxB * (kG + 2) * kRawStride;
+constexpr int kOffNormW = kOffTrig + (kD / 2) * kTrigStride * 8;  // q and k norm weights, [2][64] bf16
 constexpr int kOffPos = kOffNormW + 2 * kD * 2;      // positions of the call's tokens, [64] int64
 constexpr int kOffPlan = kOffPos + kMaxR * kMaxB * 8;
 constexpr int kNumBars = 2 * kStages + 3 * kSBufs + 2;  // full, empty, s_full[3], p_full[3], o_done[3], q_ready, done
@@ -776,8 +784,8 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         uint8_t *bk = smem + kOffBlkK;
         uint8_t *bv = smem + kOffBlkV;
         uint8_t *raw_q = smem + kOffRaw;
-        uint8_t *raw_k = raw_q + kMaxB * kG * kD * 2;
-        uint8_t *raw_v = raw_k + kMaxB * kD * 2;
+        uint8_t *raw_k = raw_q + kMaxB * kG * kRawStride;
+        uint8_t *raw_v = raw_k + kMaxB * kRawStride;
         float2 *trig = reinterpret_cast<float2 *>(smem + kOffTrig);
         const long long row_w = static_cast<long long>(p.Hq + 2 * p.Hkv) * kD;
         __nv_bfloat16 *normw = reinterpret_cast<__nv_bfloat16 *>(smem + kOffNormW);  // [0..63] q, [64..127] k
@@ -834,14 +842,14 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
             const char *qkv_rows = reinterpret_cast<const char *>(p.qkv) + static_cast<long long>(r) * p.B * row_w * 2;
             for (int e = t; e < p.B * 48; e += kRowThreads) {
                 const int ti = e / 48, c = e - ti * 48;
-                cp_async16(smem_u32(raw_q) + ti * 768 + c * 16,
+                cp_async16(smem_u32(raw_q) + (ti * kG + (c >> 3)) * kRawStride + (c & 7) * 16,
                            qkv_rows + ti * row_w * 2 + static_cast<long long>(h) * 768 + c * 16);
             }
             if (with_block) {
                 for (int e = t; e < p.B * 16; e += kRowThreads) {
                     const int ti = e >> 4, c = e & 15;
                     const long long head = c < 8 ? p.Hq + h : p.Hq + p.Hkv + h;
-                    cp_async16(smem_u32(c < 8 ? raw_k : raw_v) + ti * 128 + (c & 7) * 16,
+                    cp_async16(smem_u32(c < 8 ? raw_k : raw_v) + ti * kRawStride + (c & 7) * 16,
                                qkv_rows + ti * row_w * 2 + head * 128 + (c & 7) * 16);
                 }
             }
@@ -860,7 +868,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                         const float half_turns = static_cast<float>(static_cast<int>(turns >> 32)) * 0x1p-31f;
                         float sn, cs;
                         sincospif(half_turns, &sn, &cs);
-                        trig[e] = make_float2(cs * p.rope_mscale, sn * p.rope_mscale);
+                        trig[(e & 31) * kTrigStride + (e >> 5)] = make_float2(cs * p.rope_mscale, sn * p.rope_mscale);
                     }
                 }
             }
@@ -887,7 +895,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                     if (rix < rows) {
                         const int g = rix / p.B;
                         ti = rix - g * p.B;
-                        src = raw_q + (ti * kG + g) * 128;
+                        src = raw_q + (ti * kG + g) * kRawStride;
                         dst = qtile;
                         drow = (rix / kRowsPerQuarter) * 16 + rix % kRowsPerQuarter;
                         norm = QKNORM;
@@ -896,7 +904,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                     const int j = rix - kRows;
                     if (with_block && j < p.B) {
                         ti = j;
-                        src = raw_k + j * 128;
+                        src = raw_k + j * kRawStride;
                         dst = bk;
                         drow = j;
                         norm = QKNORM;
@@ -905,7 +913,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                 } else {
                     const int j = rix - kRows - kMaxB;
                     if (with_block && j < p.B) {
-                        src = raw_v + j * 128;
+                        src = raw_v + j * kRawStride;
                         dst = bv;
                         drow = j;
                     }
@@ -938,7 +946,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                         const int jp = 16 * hp + e;
                         const float n_lo = lo[e] * inv * __bfloat162float(w[jp]);
                         const float n_hi = hi[e] * inv * __bfloat162float(w[jp + 32]);
-                        const float2 cs = trig[ti * 32 + jp];
+                        const float2 cs = trig[jp * kTrigStride + ti];
                         lo[e] = n_lo * cs.x - n_hi * cs.y;
                         hi[e] = n_hi * cs.x + n_lo * cs.y;
                     }

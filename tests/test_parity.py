@@ -150,6 +150,15 @@ def test_rows_whose_maximum_jumps_mid_chunk(R, Hq, Hkv, L):
     assert_close(out, ref, case.name)
 
 
+def test_huge_page_stride_short_contexts():
+    """page_stride 200,000 (each unit gets 6,251 workspace slots, so slot
+    indices and the combine's reads reach ~12,500 slots deep) with short
+    contexts; the page-table rows are poison past their first 100 entries."""
+    case = workloads.build_case("stride200k", R=2, B=8, Hq=6, Hkv=1, lens=[5000, 64], page_stride=200000,
+                                used_per_row=100, num_pages=200, qknorm=True, seed=95, device="cuda")
+    check(case)
+
+
 def test_production_block_width_w6_8x6():
     check(workloads.w6_8x6(device="cuda"))
 

@@ -159,6 +159,24 @@ def test_huge_page_stride_short_contexts():
     check(case)
 
 
+def test_positions_beyond_32_bits():
+    """int64 positions near 2^33 and 2^40 in the fused attention: the angle
+    is reduced exactly as a fraction of a turn in 64-bit integers."""
+    for base_pos, seed in ((2 ** 33 + 12345, 96), (2 ** 40 - 77, 97)):
+        case = workloads.build_case("bigpos64", R=2, B=8, Hq=24, Hkv=4, lens=[300, 2041], page_stride=32,
+                                    num_pages=64, qknorm=True, pos_dtype=torch.int64, seed=seed, device="cuda")
+        case.positions = case.positions + base_pos
+        check(case)
+
+
+@pytest.mark.parametrize("rope_base,eps", [(500000.0, 1e-6), (1000.0, 1e-3)])
+def test_other_rope_base_and_eps(rope_base, eps):
+    case = workloads.build_case("base_eps", R=4, B=8, Hq=6, Hkv=1, lens=[2041, 700, 64, 0], page_stride=32,
+                                num_pages=128, qknorm=True, seed=98, device="cuda")
+    case = dataclasses.replace(case, rope_base=rope_base, eps=eps)
+    check(case)
+
+
 def test_production_block_width_w6_8x6():
     check(workloads.w6_8x6(device="cuda"))
 

@@ -177,6 +177,13 @@ def test_other_rope_base_and_eps(rope_base, eps):
     check(case)
 
 
+@pytest.mark.parametrize("scale,qknorm", [(0.2, True), (0.05, False)])
+def test_other_softmax_scales(scale, qknorm):
+    case = workloads.build_case("scale", R=3, B=5, Hq=24, Hkv=4, lens=[1500, 65, 2041], page_stride=32,
+                                num_pages=96, qknorm=qknorm, seed=99, device="cuda")
+    check(dataclasses.replace(case, scale=scale))
+
+
 def test_production_block_width_w6_8x6():
     check(workloads.w6_8x6(device="cuda"))
 

@@ -13,21 +13,26 @@
 // Design (one GPU, HBM-bound):
 //   * Work unit = (request r, kv head h).  Its items are the block (item 0,
 //     the B block keys) and its context pages (items 1..ceil(L/64)).  A unit
-//     is cut into chunks of ch(u) items, ch(u) = clamp(ceil(items/n), 1,
-//     kChunkMax) with n = max(16, ceil(304/units)), so chunk boundaries
-//     depend on that unit's length and the call's shape alone.
-//     All units' items are laid end to end; CTA c of the grid (sized to fill
-//     every SM) takes the chunks whose first item falls in the c-th equal
-//     slice of that line.  Long and short contexts thus spread over all SMs,
-//     and every chunk's partial result is the same whatever the other
-//     requests hold: requests are isolated bit for bit.  The plan is built on
-//     the device from ctx_lens, so a captured graph replays with new lengths.
+//     is cut into chunks of ch(u) items: ceil(items/n) with n = max(16,
+//     ceil(304/units)), at least min(ceil(items/16), 4), rounded up to a
+//     power of two above 4 and at most kChunkMax (unit_chunking), so chunk
+//     boundaries depend on that unit's length and the call's shape alone.
+//     All units' items are laid end to end and the line is cut into one
+//     slice per CTA of the grid (sized to fill every SM); a CTA takes the
+//     chunks that start in its slice.  When every CTA gets several of the
+//     largest chunks, the line counts each chunk as its unit's chunk size and
+//     is cut into whole-chunk slices of equal size (build_plan).  Long and
+//     short contexts thus spread over all SMs, and every chunk's partial
+//     result is the same whatever the other requests hold: requests are
+//     isolated bit for bit.  The plan is built on the device from ctx_lens,
+//     so a captured graph replays with new lengths.
 //   * The split pass (k3da_tc_kernel, below) runs on the 5th-generation
 //     tensor cores: a producer warp walks the page table (32 ids per
 //     coalesced load, a batch ahead) and TMA-loads each page's K and V tiles
 //     (64 x 64 bf16, 8 KB each, contiguous in the HND pool, 128-byte
-//     swizzle) into a ring of shared-memory stages; one warp issues
-//     S = Q K^T and another O += P V as tcgen05.mma with TMEM accumulators;
+//     swizzle) into a 5-stage ring in shared memory; one warp issues
+//     S = Q K^T and another O += P V as M = 64 tcgen05.mma with TMEM
+//     accumulators (three S/P buffers, so QK^T runs up to two pages ahead);
 //     four row warps run the online softmax (base 2, scale folded in, lazy
 //     rescale) and hand P to the P.V product through TMEM.
 //   * When a CTA starts on a unit, its q (and block k, v) rows are staged

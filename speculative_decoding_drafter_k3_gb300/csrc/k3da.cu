@@ -1120,7 +1120,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
 // the split pass.
 constexpr int kCombineRows = 2;
 constexpr int kCombineLanes = 8;
-constexpr int kCombineFold = 4;
+constexpr int kCombineFold = 2;
 
 __global__ void __launch_bounds__(128, 6) k3da_combine_kernel(const __grid_constant__ Params p) {
     const int per_unit = kRows / kCombineRows;

@@ -1119,10 +1119,11 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
 // fixed slots, and griddepcontrol.wait orders every workspace read after
 // the split pass.
 constexpr int kCombineRows = 2;
+constexpr int kCombineThreads = 64 * kCombineRows;  // (row, 8 dims, chunk lane) per thread
 constexpr int kCombineLanes = 8;
 constexpr int kCombineFold = 2;
 
-__global__ void __launch_bounds__(128, 6) k3da_combine_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kCombineThreads, 768 / kCombineThreads) k3da_combine_kernel(const __grid_constant__ Params p) {
     const int per_unit = kRows / kCombineRows;
     const int u = blockIdx.x / per_unit;
     const int row = (blockIdx.x - u * per_unit) * kCombineRows + (threadIdx.x >> 6);
@@ -1499,7 +1500,7 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
     cudaLaunchConfig_t lc;
     memset(&lc, 0, sizeof lc);
     lc.gridDim = dim3(static_cast<unsigned>(R * Hkv * (kRows / kCombineRows)));
-    lc.blockDim = dim3(128);
+    lc.blockDim = dim3(kCombineThreads);
     lc.dynamicSmemBytes = 0;
     lc.stream = st;
     cudaLaunchAttribute attr[1];

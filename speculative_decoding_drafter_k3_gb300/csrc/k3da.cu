@@ -1363,7 +1363,7 @@ constexpr size_t workspace_slots(int R, int Hkv, int page_stride) {
     return static_cast<size_t>(R) * Hkv * static_cast<size_t>(slots_per_unit(R, Hkv, page_stride));
 }
 
-constexpr size_t kWsHeaderBytes = 512;  // reserved; the partials start here (256-byte aligned)
+constexpr size_t kWsHeaderBytes = 512;  // reserved; the partials follow (16-byte aligned, as the workspace is)
 constexpr size_t kSlotBytes = kPartialElems * 2 + kRows * 8;  // bf16 O, then (m, l) fp32 per row
 
 constexpr size_t workspace_for(int R, int Hkv, int page_stride) {

@@ -30,13 +30,13 @@
 //     tensor cores: a producer warp walks the page table (32 ids per
 //     coalesced load, a batch ahead) and TMA-loads each page's K and V tiles
 //     (64 x 64 bf16, 8 KB each, contiguous in the HND pool, 128-byte
-//     swizzle) into a 5-stage ring in shared memory; one warp issues
+//     swizzle) into a 6-stage ring in shared memory; one warp issues
 //     S = Q K^T and another O += P V as M = 64 tcgen05.mma with TMEM
 //     accumulators (three S/P buffers, so QK^T runs up to two pages ahead);
 //     four row warps run the online softmax (base 2, scale folded in, lazy
 //     rescale) and hand P to the P.V product through TMEM.
-//   * When a CTA starts on a unit, its q (and block k, v) rows are staged
-//     with one batch of cp.async copies and turned into operand tiles:
+//   * When a CTA starts on a unit, each row thread loads its q (or block k,
+//     v) row's pieces straight from qkv into registers and writes operand tiles:
 //     RMSNorm and RoPE happen on the way in.  A RoPE angle is reduced
 //     exactly in integer arithmetic (position times a 64-bit fixed-point
 //     turn rate, wrapping), then turned by an accurate sincospif.
@@ -404,14 +404,6 @@ __device__ void build_plan(const Params &p, Plan *pl, int cta, int C, bool repor
     if (lane == 0) pl->nrun = __popc(mask);
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
-
 // ---------------------------------------------------- tcgen05 split pass --
 //
 // The two contractions run on the 5th-generation tensor cores.  An item is
@@ -438,7 +430,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // P <= 256 is exact enough in bf16 and fp32), so the common path never
 // touches O.
 namespace tc {
-constexpr int kStages = 5;
+constexpr int kStages = 6;
 constexpr int kRowWarps = 4;  // one warp per TMEM lane quarter
 constexpr int kRowThreads = 32 * kRowWarps;
 constexpr int kRowsPerQuarter = 12;
@@ -462,19 +454,12 @@ constexpr int kBlkRows = 16;                          // block tiles: B <= 8 key
 constexpr int kQRows = 64;                            // M of the MMAs: rows 16q..16q+15 -> TMEM lanes 32q..32q+15
 constexpr int kOffBlkK = kOffQ + kQRows * 128;        // kBlkRows rows x 128 B
 constexpr int kOffBlkV = kOffBlkK + kBlkRows * 128;  // kBlkRows rows x 128 B
-// Raw q [8][6], k [8] and v [8] rows of 128 B, each at a 144-byte stride: the
-// two threads of a row read it in 16-byte pieces, and at a 128-byte stride
-// (or the 768-byte one of a token's six q rows) the 16 rows of a warp would
-// all fall on the same four banks.
-constexpr int kRawStride = 144;
-constexpr int kOffRaw = kOffBlkV + kBlkRows * 128;
 // RoPE (cos, sin) of pair j and token i at [j][i], kMaxB + 1 entries per
 // pair: a warp's rows read one pair for up to 8 tokens at a time.
 constexpr int kTrigStride = kMaxB + 1;
-constexpr int kOffTrig = kOffRaw + kMaxB * (kG + 2) * kRawStride;
+constexpr int kOffTrig = kOffBlkV + kBlkRows * 128;
 constexpr int kOffNormW = kOffTrig + (kD / 2) * kTrigStride * 8;  // q and k norm weights, [2][64] bf16
-constexpr int kOffPos = kOffNormW + 2 * kD * 2;      // positions of the call's tokens, [64] int64
-constexpr int kOffPlan = kOffPos + kMaxR * kMaxB * 8;
+constexpr int kOffPlan = kOffNormW + 2 * kD * 2;
 constexpr int kNumBars = 2 * kStages + 3 * kSBufs + 2;  // full, empty, s_full[3], p_full[3], o_done[3], q_ready, done
 constexpr int kOffBar = kOffPlan + (static_cast<int>(sizeof(Plan)) + 15) / 16 * 16;
 constexpr int kOffTaddr = kOffBar + kNumBars * 8;
@@ -577,9 +562,11 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
 
     // The norm weights and the positions of all the call's tokens do not
     // depend on the plan: their loads are issued first and land while the
-    // plan is built (they go to shared memory once the row warps start).
+    // plan is built (the weights go to shared memory once the row warps
+    // start; row warps 1-3, which form the RoPE angles, keep the positions
+    // in registers and share them by shuffle).
     __nv_bfloat16 w_early = __float2bfloat16_rn(0.f);
-    long long pos_early = 0;
+    long long pos_lo = 0, pos_hi = 0;  // row warps 1-3: positions of tokens lane and lane + 32
     // A row thread's RoPE pair is j = its lane (every angle it forms): its
     // turn rate, read with constant indices (a lane-dependent index into the
     // kernel parameters would serialize the warp's reads) and early (the
@@ -589,10 +576,14 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     unsigned long long my_rate = 0;
     if (QKNORM && threadIdx.x < kRowThreads) {
         w_early = threadIdx.x < kD ? p.q_w[threadIdx.x] : p.k_w[threadIdx.x - kD];
-        if (threadIdx.x < p.R * p.B)
-            pos_early = p.pos_i64 ? reinterpret_cast<const long long *>(p.positions)[threadIdx.x]
-                                  : reinterpret_cast<const int *>(p.positions)[threadIdx.x];
         if (warp != 0) {
+            const int nt = p.R * p.B;
+            if (lane < nt)
+                pos_lo = p.pos_i64 ? reinterpret_cast<const long long *>(p.positions)[lane]
+                                   : reinterpret_cast<const int *>(p.positions)[lane];
+            if (lane + 32 < nt)
+                pos_hi = p.pos_i64 ? reinterpret_cast<const long long *>(p.positions)[lane + 32]
+                                   : reinterpret_cast<const int *>(p.positions)[lane + 32];
 #pragma unroll
             for (int j = 0; j < kD / 2; ++j)
                 if (lane == j) my_rate = p.turn_rate[j];
@@ -788,16 +779,11 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         uint8_t *qtile = smem + kOffQ;
         uint8_t *bk = smem + kOffBlkK;
         uint8_t *bv = smem + kOffBlkV;
-        uint8_t *raw_q = smem + kOffRaw;
-        uint8_t *raw_k = raw_q + kMaxB * kG * kRawStride;
-        uint8_t *raw_v = raw_k + kMaxB * kRawStride;
         float2 *trig = reinterpret_cast<float2 *>(smem + kOffTrig);
         const long long row_w = static_cast<long long>(p.Hq + 2 * p.Hkv) * kD;
         __nv_bfloat16 *normw = reinterpret_cast<__nv_bfloat16 *>(smem + kOffNormW);  // [0..63] q, [64..127] k
-        long long *pos_s = reinterpret_cast<long long *>(smem + kOffPos);            // [R*B]
         if (QKNORM) {
             normw[t] = w_early;
-            if (t < p.R * p.B) pos_s[t] = pos_early;
         }
 
         // A chunk's partial is written while the next chunk's first item is in
@@ -845,18 +831,51 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
             // ---- stage and build this unit's Q (and block K, V) tiles.
             named_bar_sync(1, kRowThreads);
             const char *qkv_rows = reinterpret_cast<const char *>(p.qkv) + static_cast<long long>(r) * p.B * row_w * 2;
-            for (int e = t; e < p.B * 48; e += kRowThreads) {
-                const int ti = e / 48, c = e - ti * 48;
-                cp_async16(smem_u32(raw_q) + (ti * kG + (c >> 3)) * kRawStride + (c & 7) * 16,
-                           qkv_rows + ti * row_w * 2 + static_cast<long long>(h) * 768 + c * 16);
-            }
-            if (with_block) {
-                for (int e = t; e < p.B * 16; e += kRowThreads) {
-                    const int ti = e >> 4, c = e & 15;
-                    const long long head = c < 8 ? p.Hq + h : p.Hq + p.Hkv + h;
-                    cp_async16(smem_u32(c < 8 ? raw_k : raw_v) + ti * kRawStride + (c & 7) * 16,
-                               qkv_rows + ti * row_w * 2 + head * 128 + (c & 7) * 16);
+            // Two threads per row: thread t takes row t/2 and the 16 RoPE
+            // pairs (j, j+32) with j in [16*(t&1), 16*(t&1)+16).  Rows 0..47
+            // are query rows (g*B + i), 48..55 block keys, 56..63 block
+            // values.  The row's four 16-byte pieces come straight from qkv
+            // into registers, issued now so they land during the angles.
+            const int rix = t >> 1, hp = t & 1;
+            const char *src = nullptr;
+            uint8_t *dst = nullptr;
+            int drow = 0, ti = 0;
+            bool norm = false;
+            const __nv_bfloat16 *w = normw;
+            if (rix < kRows) {
+                if (rix < rows) {
+                    const int g = rix / p.B;
+                    ti = rix - g * p.B;
+                    src = qkv_rows + ti * row_w * 2 + static_cast<long long>(h * kG + g) * 128;
+                    dst = qtile;
+                    drow = (rix / kRowsPerQuarter) * 16 + rix % kRowsPerQuarter;
+                    norm = QKNORM;
                 }
+            } else if (rix < kRows + kMaxB) {
+                const int j = rix - kRows;
+                if (with_block && j < p.B) {
+                    ti = j;
+                    src = qkv_rows + j * row_w * 2 + static_cast<long long>(p.Hq + h) * 128;
+                    dst = bk;
+                    drow = j;
+                    norm = QKNORM;
+                    w = normw + kD;
+                }
+            } else {
+                const int j = rix - kRows - kMaxB;
+                if (with_block && j < p.B) {
+                    src = qkv_rows + j * row_w * 2 + static_cast<long long>(p.Hq + p.Hkv + h) * 128;
+                    dst = bv;
+                    drow = j;
+                }
+            }
+            uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, b0 = a0, b1 = a0;
+            if (src != nullptr) {
+                const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+                a0 = __ldg(s4 + 2 * hp);
+                a1 = __ldg(s4 + 2 * hp + 1);
+                b0 = __ldg(s4 + 4 + 2 * hp);
+                b1 = __ldg(s4 + 4 + 2 * hp + 1);
             }
             if (QKNORM && warp != 0) {
                 // Row warps 1-3 form the B x 32 (token, pair) angles, three
@@ -864,12 +883,15 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
 #pragma unroll
                 for (int k3 = 0; k3 < 3; ++k3) {
                     const int e = (t - 32) + 96 * k3;
+                    const int tok = r * p.B + (e >> 5);
+                    const long long plo = __shfl_sync(kFull, pos_lo, tok & 31);
+                    const long long phi = __shfl_sync(kFull, pos_hi, tok & 31);
                     if (e < p.B * 32) {
                         // The angle's fraction of a turn, exactly (integer
                         // arithmetic wraps whole turns away); its top 32
                         // bits are the signed fraction in [-1/2, 1/2).
                         const unsigned long long turns =
-                            static_cast<unsigned long long>(pos_s[r * p.B + (e >> 5)]) * my_rate;
+                            static_cast<unsigned long long>(tok < 32 ? plo : phi) * my_rate;
                         const float half_turns = static_cast<float>(static_cast<int>(turns >> 32)) * 0x1p-31f;
                         float sn, cs;
                         sincospif(half_turns, &sn, &cs);
@@ -877,7 +899,6 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                     }
                 }
             }
-            cp_async_wait_all();
             if (it > 0) {
                 // The block tiles are rewritten below: the last P.V (which
                 // may have read the previous block's V) must be complete.
@@ -886,47 +907,9 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                 fence_after();
             }
             named_bar_sync(1, kRowThreads);
-            // Two threads per row: thread t takes row t/2 and the 16 RoPE
-            // pairs (j, j+32) with j in [16*(t&1), 16*(t&1)+16).  Rows 0..47
-            // are query rows (g*B + i), 48..55 block keys, 56..63 block values.
             {
-                const int rix = t >> 1, hp = t & 1;
-                const uint8_t *src = nullptr;
-                uint8_t *dst = nullptr;
-                int drow = 0, ti = 0;
-                bool norm = false;
-                const __nv_bfloat16 *w = normw;
-                if (rix < kRows) {
-                    if (rix < rows) {
-                        const int g = rix / p.B;
-                        ti = rix - g * p.B;
-                        src = raw_q + (ti * kG + g) * kRawStride;
-                        dst = qtile;
-                        drow = (rix / kRowsPerQuarter) * 16 + rix % kRowsPerQuarter;
-                        norm = QKNORM;
-                    }
-                } else if (rix < kRows + kMaxB) {
-                    const int j = rix - kRows;
-                    if (with_block && j < p.B) {
-                        ti = j;
-                        src = raw_k + j * kRawStride;
-                        dst = bk;
-                        drow = j;
-                        norm = QKNORM;
-                        w = normw + kD;
-                    }
-                } else {
-                    const int j = rix - kRows - kMaxB;
-                    if (with_block && j < p.B) {
-                        src = raw_v + j * kRawStride;
-                        dst = bv;
-                        drow = j;
-                    }
-                }
                 float lo[16], hi[16];
                 if (src != nullptr) {
-                    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-                    const uint4 a0 = s4[2 * hp], a1 = s4[2 * hp + 1], b0 = s4[4 + 2 * hp], b1 = s4[4 + 2 * hp + 1];
                     const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
                     const uint32_t bv2[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll

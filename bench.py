@@ -4,6 +4,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload long_context|mixed_8x8|heads_24_4|tiny|w6_8x6|single_w6|...]
                     [--yarn] [--op attn|qk_norm_rope] [--warm-l2] [--no-e2e] [--no-cpu-baseline]
+                    [--sweep]
 
 Metric: drafter block-attention microseconds per call (lower is better) on
 one of the op's workloads, default the long-context one (8 requests x 8 draft
@@ -14,10 +15,12 @@ the dominant kernel against the measured copy bandwidth in "roofline".
 ours:       the CUDA library through its Python binding.  Inputs are resident
             in HBM; L2 is flushed (512 MB written, then 512 MB read) before
             every timed call; each call is timed with CUDA events on the
-            launching stream.  "e2e" times the same call with the per-step
-            inputs (qkv, page table, lengths, positions) copied from pinned
-            host memory in one packed copy and the output copied back, inside
-            the timed region.  --warm-l2 skips the flush (a warm-cache line,
+            launching stream.  "e2e" times the same call handed the per-step
+            inputs (qkv, page table, lengths, positions) and the output in
+            pinned host memory: the kernels read and write them across the
+            host link inside the timed region.  "e2e_copies" times it with
+            the inputs copied to device memory in one packed copy and the
+            output copied back instead.  --warm-l2 skips the flush (a warm-cache line,
             labelled in "config").  "cpu_baseline" is one whole call of the
             fp64 oracle on one host thread; "cpu_all_cores" is one whole call
             of it on all host cores.
@@ -32,6 +35,7 @@ the job's aggregate time per call (max-over-ranks time / calls of all ranks).
 from __future__ import annotations
 
 import argparse
+import functools
 import gc
 import hashlib
 import json
@@ -76,6 +80,10 @@ def parse():
     ap.add_argument("--warm-l2", action="store_true",
                     help="do not flush L2 between timed calls (a labelled warm-cache line, "
                          "never the headline)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the headline: time every other configuration (tiny, the "
+                         "8x8 and W=6 shapes, each request x token split) with L2 flushed and "
+                         "warm, one JSON line")
     return ap.parse_args()
 
 
@@ -290,6 +298,37 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args, k3da, workloads, dev, status, flush, timed_calls):
+    """Every configuration but the long-context one, whole calls timed as
+    the headline is (events on the launching stream, K calls), once with L2
+    flushed before each call and once warm (the previous call's inputs left
+    in L2, a spin kernel in front of each call): one JSON line."""
+    cases = [("tiny", workloads.tiny), ("mixed_8x8", workloads.mixed_8x8),
+             ("heads_24_4", workloads.heads_24_4), ("w6_8x6", workloads.w6_8x6),
+             ("single_w6", workloads.single_w6), ("single_w6_long", workloads.single_w6_long)]
+    cases += [(f"split_{r}x{b}", functools.partial(workloads.split_sweep, r, b))
+              for r, b in workloads.SPLITS]
+    rows = {}
+    for name, make in cases:
+        c = make(device=dev)
+        o = torch.empty(c.T, c.Hq * c.D, dtype=torch.bfloat16, device=dev)
+        w = k3da.case_workspace(c)
+        row = {"algorithmic_bytes": c.algorithmic_bytes()}
+        for warm in (False, True):
+            flush.warm = warm
+            ms = sorted(timed_calls(c, o, w, args.steps))
+            row["warm" if warm else "cold"] = {
+                "us_mean": statistics.mean(ms) * 1e3, "us_median": statistics.median(ms) * 1e3,
+                "us_p10": ms[len(ms) // 10] * 1e3, "us_p90": ms[(9 * len(ms)) // 10] * 1e3}
+        rows[name] = row
+    flush.warm = args.warm_l2
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    print(json.dumps({"sweep": rows, "unit": UNIT, "steps": args.steps, "warmup": args.warmup,
+                      "timing": "whole calls, CUDA events on the launching stream; cold = L2 "
+                                "flushed before each call, warm = previous call's inputs in L2"}),
+          flush=True)
+
+
 def run_ours(args, world, rank):
     import speculative_decoding_drafter_k3_gb300 as k3da
     from speculative_decoding_drafter_k3_gb300 import build as kbuild, workloads
@@ -306,12 +345,13 @@ def run_ours(args, world, rank):
     sink = torch.empty((), dtype=torch.float32, device=dev)
 
     class _Flush:
-        @staticmethod
-        def zero_():
+        warm = args.warm_l2
+
+        def zero_(self):
             # Write a buffer larger than L2, then read another one: L2 ends
             # up holding clean lines of neither input, so the timed call
             # neither hits in L2 nor pays for writing back the flush.
-            if args.warm_l2:
+            if self.warm:
                 # No flush: a spin kernel that touches no memory keeps the
                 # GPU busy while the host enqueues the call, so the timed
                 # call is not waiting for its own launch.
@@ -356,6 +396,9 @@ def run_ours(args, world, rank):
         return [e[0].elapsed_time(e[1]) for e in ev]
 
     K = args.steps
+    if args.sweep:
+        run_sweep(args, k3da, workloads, dev, status, flush, timed_calls)
+        return
     # Headline: whole calls (split pass + combine), one event pair per call.
     clocks = ClockSampler(dev.index) if rank == 0 else None
     call_ms = timed_calls(case, out, ws, K, clocks)
@@ -397,11 +440,14 @@ def run_ours(args, world, rank):
                            "algorithmic_bytes": c.algorithmic_bytes()}
         assert int(status.item()) == 0, f"device status {int(status.item())}"
 
-    # End to end through the public binding with host buffers: the step's
-    # inputs (qkv, page table, lengths, positions) travel from pinned host
-    # memory in one packed copy, the call reads them in place, and the output
-    # comes back in one copy.
-    e2e = None
+    # End to end through the public binding with host buffers, two ways.
+    # Host-resident ("e2e"): the call is handed the pinned host tensors
+    # themselves (qkv, page table, lengths, positions, output); its kernels
+    # read the inputs and write the output across the host link, with no
+    # copy.  Copies ("e2e_copies"): the inputs travel from pinned host memory
+    # in one packed copy, the call reads them in device memory, and the
+    # output comes back in one copy.
+    e2e = e2e_copies = None
     if not args.no_e2e:
         import dataclasses
         inputs = [case.qkv, case.page_table, case.ctx_lens] + ([case.positions] if case.qknorm else [])
@@ -412,40 +458,55 @@ def run_ours(args, world, rank):
             total += t.numel() * t.element_size()
         dev_pack = torch.empty(total, dtype=torch.uint8, device=dev)
         host_pack = torch.zeros(total, dtype=torch.uint8).pin_memory()
-        views = []
+        views, host_views = [], []
         for t, o in zip(inputs, offs):
             n = t.numel() * t.element_size()
             host_pack[o:o + n].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
             views.append(dev_pack[o:o + n].view(t.dtype).view(t.shape))
+            host_views.append(host_pack[o:o + n].view(t.dtype).view(t.shape))
         case_e2e = dataclasses.replace(case, qkv=views[0], page_table=views[1], ctx_lens=views[2],
                                        positions=views[3] if case.qknorm else None)
+        case_host = dataclasses.replace(case, qkv=host_views[0], page_table=host_views[1],
+                                        ctx_lens=host_views[2], positions=host_views[3] if case.qknorm else None)
         host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
 
-        def step_e2e():
+        def step_copies():
             dev_pack.copy_(host_pack, non_blocking=True)
             k3da.run_case(case_e2e, out=out, workspace=ws, status=status, yarn=yarn)
             host_out.copy_(out, non_blocking=True)
 
-        for _ in range(3):
-            step_e2e()
-        torch.cuda.synchronize()
-        eev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-        barrier(world)
-        torch.cuda.synchronize()
-        gc.disable()
-        for i in range(K):
-            flush.zero_()
-            eev[i][0].record()
-            step_e2e()
-            eev[i][1].record()
-        torch.cuda.synchronize()
-        gc.enable()
-        barrier(world)
-        e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in eev), world)
-        e2e = {"value": e2e_ms * 1e3 / (K * world), "unit": UNIT,
-               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in inputs),
-               "d2h_bytes_per_step": out.numel() * out.element_size(),
-               "copies_per_step": {"h2d": 1, "d2h": 1}}
+        def step_host():
+            k3da.run_case(case_host, out=host_out, workspace=ws, status=status, yarn=yarn)
+
+        def time_steps(step):
+            for _ in range(3):
+                step()
+            torch.cuda.synchronize()
+            eev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+            barrier(world)
+            torch.cuda.synchronize()
+            gc.disable()
+            for i in range(K):
+                flush.zero_()
+                eev[i][0].record()
+                step()
+                eev[i][1].record()
+            torch.cuda.synchronize()
+            gc.enable()
+            barrier(world)
+            return max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in eev), world) * 1e3 / (K * world)
+
+        h2d = sum(t.numel() * t.element_size() for t in inputs)
+        d2h = out.numel() * out.element_size()
+        e2e = {"value": time_steps(step_host), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "copies_per_step": {"h2d": 0, "d2h": 0},
+               "transfer": "host-resident: the call is handed the pinned host tensors; its kernels "
+                           "read the inputs and write the output across the host link"}
+        e2e_copies = {"value": time_steps(step_copies), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h, "copies_per_step": {"h2d": 1, "d2h": 1},
+                      "transfer": "one packed cudaMemcpyAsync of the inputs to device memory, the "
+                                  "call, one copy of the output back"}
+        assert int(status.item()) == 0, f"device status {int(status.item())}"
 
     out_bytes = case.T * case.Hq * case.D * 2
     split_bytes = case.algorithmic_bytes() - out_bytes
@@ -470,7 +531,7 @@ def run_ours(args, world, rank):
                                                  "in L2 from the previous call)"} if args.warm_l2 else {}),
                                        "rope": "yarn(4.0, 4096, 32, 1)" if yarn is not None else "neox",
                                        "split_ctas": k3da.split_grid(dev.index)}),
-            "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clock_info,
+            "roofline": roofline, "e2e": e2e, "e2e_copies": e2e_copies, "gpu_launches": 2 * K, "clocks": clock_info,
             "small_workloads": small,
             "median_call_us": statistics.median(call_ms) * 1e3,
             "p10_p90_call_us": [sorted(call_ms)[int(0.1 * (K - 1))] * 1e3,

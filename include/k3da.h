@@ -19,7 +19,14 @@
  * tokens per page, S = page stride (entries per page-table row), G = Hq/Hkv.
  *
  * Memory.  Every pointer is DEVICE memory owned by the caller, except where
- * a comment says otherwise.  The library allocates nothing, keeps no
+ * a comment says otherwise.  out, qkv, page_table, ctx_lens and positions
+ * may instead be pinned HOST memory that the GPU addresses directly (from
+ * cudaHostAlloc / cudaMallocHost, or registered with cudaHostRegister, on a
+ * system with unified addressing): the kernels then read those inputs and
+ * write the output across the host link (NVLink-C2C on a Grace host) with
+ * no separate copy; the output is in host memory once the call's work on
+ * the stream is complete.  kv_pool, the norm weights, workspace and status
+ * are always device memory.  The library allocates nothing, keeps no
  * per-call state, never synchronises and never reads device data on the
  * host: lengths, page table, positions and qkv are read by the kernels, so a
  * call captured in a CUDA graph replays with those buffers rewritten.  The

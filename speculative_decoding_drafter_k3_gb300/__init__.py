@@ -2,7 +2,8 @@
 
 The compute lives in ``libk3da.so`` (hand-written CUDA, C ABI declared in
 ``include/k3da.h``).  This module only marshals torch tensors into that ABI:
-device pointers, sizes, dtype codes and the current CUDA stream.  There is no
+pointers (device memory, or pinned host memory where the ABI allows it),
+sizes, dtype codes and the current CUDA stream.  There is no
 CPU fallback: if the library is missing, every call raises.
 
 Operation (page "[None][feat] Share Kimi K3 FP4 modeling and add NVFP4
@@ -138,11 +139,26 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _device_or_pinned(name, t):
+    """out, qkv, page_table, ctx_lens and positions may live in pinned host
+    memory, which the kernels read (or write) across the host link."""
+    if not (t.is_cuda or t.is_pinned()) or not t.is_contiguous():
+        raise K3daError(f"{name} must be a contiguous CUDA tensor or a contiguous pinned host tensor")
+
+
+def _device_scratch(workspace, status):
+    """The workspace and the status word are always device memory."""
+    if workspace is not None and (not workspace.is_cuda or not workspace.is_contiguous()):
+        raise K3daError("workspace must be a contiguous CUDA tensor")
+    if status is not None and (not status.is_cuda or status.dtype != torch.int32):
+        raise K3daError("status must be an int32 CUDA tensor")
+
+
 def _shape_args(out, qkv, kv_pool, page_table, ctx_lens, block_len, num_q_heads, num_kv_heads):
-    for name, t in [("out", out), ("qkv", qkv), ("kv_pool", kv_pool), ("page_table", page_table),
-                    ("ctx_lens", ctx_lens)]:
-        if not t.is_cuda or not t.is_contiguous():
-            raise K3daError(f"{name} must be a contiguous CUDA tensor")
+    for name, t in [("out", out), ("qkv", qkv), ("page_table", page_table), ("ctx_lens", ctx_lens)]:
+        _device_or_pinned(name, t)
+    if not kv_pool.is_cuda or not kv_pool.is_contiguous():
+        raise K3daError("kv_pool must be a contiguous CUDA tensor")
     if qkv.dtype != torch.bfloat16 or out.dtype != torch.bfloat16 or kv_pool.dtype != torch.bfloat16:
         raise K3daError("qkv, out and kv_pool must be bf16")
     if page_table.dtype != torch.int32 or ctx_lens.dtype != torch.int32:
@@ -159,6 +175,20 @@ def _shape_args(out, qkv, kv_pool, page_table, ctx_lens, block_len, num_q_heads,
     return R, kv_pool.shape[0], page_table.shape[1], D
 
 
+def _qknorm_args(positions, q_norm_w, k_norm_w, T, D):
+    """Checks the fused variant's extra tensors; returns the positions' dtype code."""
+    if positions.dtype not in (torch.int32, torch.int64) or positions.numel() != T:
+        raise K3daError("positions must be [T] int32 or int64")
+    _device_or_pinned("positions", positions)
+    for name, t in [("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)]:
+        if not t.is_cuda or not t.is_contiguous():
+            raise K3daError(f"{name} must be a contiguous CUDA tensor")
+    if q_norm_w.dtype != torch.bfloat16 or k_norm_w.dtype != torch.bfloat16 or \
+            q_norm_w.numel() != D or k_norm_w.numel() != D:
+        raise K3daError("norm weights must be [64] bf16")
+    return POS_I64 if positions.dtype == torch.int64 else POS_I32
+
+
 def k3da_attn(out, qkv, kv_pool, page_table, ctx_lens, *, block_len: int, num_q_heads: int,
               num_kv_heads: int, softmax_scale: float = 0.125, workspace, status=None,
               stream=None):
@@ -166,6 +196,7 @@ def k3da_attn(out, qkv, kv_pool, page_table, ctx_lens, *, block_len: int, num_q_
     lib = load_library()
     R, num_pages, S, D = _shape_args(out, qkv, kv_pool, page_table, ctx_lens, block_len,
                                      num_q_heads, num_kv_heads)
+    _device_scratch(workspace, status)
     rc = lib.k3da_attn(_ptr(out), _ptr(qkv), _ptr(kv_pool), num_pages, _ptr(page_table), S,
                        _ptr(ctx_lens), R, block_len, num_q_heads, num_kv_heads, D,
                        float(softmax_scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -183,15 +214,8 @@ def k3da_attn_qknorm(out, qkv, kv_pool, page_table, ctx_lens, positions, q_norm_
     lib = load_library()
     R, num_pages, S, D = _shape_args(out, qkv, kv_pool, page_table, ctx_lens, block_len,
                                      num_q_heads, num_kv_heads)
-    if positions.dtype not in (torch.int32, torch.int64) or positions.numel() != R * block_len:
-        raise K3daError("positions must be [T] int32 or int64")
-    for name, t in [("positions", positions), ("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)]:
-        if not t.is_cuda or not t.is_contiguous():
-            raise K3daError(f"{name} must be a contiguous CUDA tensor")
-    if q_norm_w.dtype != torch.bfloat16 or k_norm_w.dtype != torch.bfloat16 or \
-            q_norm_w.numel() != D or k_norm_w.numel() != D:
-        raise K3daError("norm weights must be [64] bf16")
-    pos_code = POS_I64 if positions.dtype == torch.int64 else POS_I32
+    _device_scratch(workspace, status)
+    pos_code = _qknorm_args(positions, q_norm_w, k_norm_w, R * block_len, D)
     args = [_ptr(out), _ptr(qkv), _ptr(kv_pool), num_pages, _ptr(page_table), S, _ptr(ctx_lens), R,
             block_len, num_q_heads, num_kv_heads, D, float(softmax_scale), _ptr(positions), pos_code,
             _ptr(q_norm_w), _ptr(k_norm_w), float(eps), float(rope_base)]
@@ -248,8 +272,9 @@ def case_workspace(case) -> torch.Tensor:
 
 
 def run_case(case, out=None, workspace=None, status=None, stream=None, yarn=None):
-    """Run the op on a ``workloads.Case`` whose tensors are on the GPU
-    (``yarn``: YaRN RoPE for the fused variant)."""
+    """Run the op on a ``workloads.Case`` whose pool and norm weights are on
+    the GPU; its qkv, page table, lengths and positions may be pinned host
+    tensors (``yarn``: YaRN RoPE for the fused variant)."""
     if out is None:
         out = torch.empty(case.T, case.Hq * case.D, dtype=torch.bfloat16, device=case.qkv.device)
     if workspace is None:
@@ -288,9 +313,8 @@ def k3da_attn_qknorm_noalloc(out, qkv, kv_pool, page_table, ctx_lens, positions,
     lib = load_library()
     R, num_pages, S, D = _shape_args(out, qkv, kv_pool, page_table, ctx_lens, block_len,
                                      num_q_heads, num_kv_heads)
-    if positions.dtype not in (torch.int32, torch.int64) or positions.numel() != R * block_len:
-        raise K3daError("positions must be [T] int32 or int64")
-    pos_code = POS_I64 if positions.dtype == torch.int64 else POS_I32
+    _device_scratch(None, status)
+    pos_code = _qknorm_args(positions, q_norm_w, k_norm_w, R * block_len, D)
     rc = lib.k3da_attn_qknorm_noalloc(_ptr(out), _ptr(qkv), _ptr(kv_pool), num_pages, _ptr(page_table),
                                       S, _ptr(ctx_lens), R, block_len, num_q_heads, num_kv_heads, D,
                                       float(softmax_scale), _ptr(positions), pos_code, _ptr(q_norm_w),

@@ -24,9 +24,13 @@
  * cudaHostAlloc / cudaMallocHost, or registered with cudaHostRegister, on a
  * system with unified addressing): the kernels then read those inputs and
  * write the output across the host link (NVLink-C2C on a Grace host) with
- * no separate copy; the output is in host memory once the call's work on
- * the stream is complete.  kv_pool, the norm weights, workspace and status
- * are always device memory.  The library allocates nothing, keeps no
+ * no cudaMemcpy.  When qkv, positions or ctx_lens are host-resident, one
+ * small kernel first copies the three into the workspace (qkv is read by
+ * every CTA working on a request, so it crosses the link once instead of
+ * many times) and the split pass starts as its programmatic dependent; the
+ * page table is read in place.  The output is in host memory once the
+ * call's work on the stream is complete.  kv_pool, the norm weights,
+ * workspace and status are always device memory.  The library allocates nothing, keeps no
  * per-call state, never synchronises and never reads device data on the
  * host: lengths, page table, positions and qkv are read by the kernels, so a
  * call captured in a CUDA graph replays with those buffers rewritten.  The
@@ -72,7 +76,10 @@ typedef enum { K3DA_POS_I32 = 0, K3DA_POS_I64 = 1 } k3da_pos_dtype;
 /*
  * Bytes of device workspace a call with these sizes needs.  Returns 0 when
  * the sizes are out of contract.  The value does not depend on lengths or on
- * the device, so one buffer serves every call of a captured graph.
+ * the device, so one buffer serves every call of a captured graph.  It holds
+ * the chunk partials and, after them, room to stage host-resident inputs
+ * (the qkv of the largest call of this head layout, 64 positions and the
+ * lengths).
  */
 size_t k3da_workspace_bytes(int num_requests, int block_len, int num_q_heads,
                             int num_kv_heads, int page_stride);
@@ -174,8 +181,10 @@ int k3da_set_phase_event(void *event);
  * without workspace / workspace_bytes; the caller still passes every input
  * and output.
  *
- * - Sizes whose workspace (k3da_workspace_bytes) exceeds the array are
- *   refused with K3DA_EWORKSPACE: page_stride <= 1279 always fits.
+ * - Sizes whose chunk partials exceed the array are refused with
+ *   K3DA_EWORKSPACE: page_stride <= 1279 always fits.  Host-resident
+ *   inputs are staged only where the array also has room for the staging
+ *   area of k3da_workspace_bytes; otherwise the kernels read them in place.
  * - Nothing is allocated or freed, by the library or by any routine it
  *   calls.
  * - The first call on a device looks up the array's device address (with

@@ -73,6 +73,20 @@ constexpr int kChunkSplits = 16;   // a unit is cut into at most this many chunk
 constexpr int kChunkTarget = 304;  // ... or, with few units, about this many chunks in all
 constexpr int kChunkMax = 32;      // ... of at most this many pages, beyond which it gets more chunks
 constexpr int kPartialElems = kRows * kD;     // O of one chunk, bf16
+// Workspace: a reserved header, the chunk partials (slot u * slots_per_unit
+// + j: bf16 O, then (m, l) fp32 per row), then room to stage host-resident
+// inputs (k3da_stage_kernel): qkv sized for the largest call of the head
+// layout, so that the workspace never depends on R or B beyond the
+// partials, then the positions (at most 64 int64) and the lengths.
+constexpr size_t kWsHeaderBytes = 512;  // the partials follow, 16-byte aligned as the workspace is
+constexpr size_t kSlotBytes = kPartialElems * 2 + kRows * 8;
+__host__ __device__ constexpr size_t staging_qkv_bytes(int Hq, int Hkv) {
+    return static_cast<size_t>(kMaxR) * kMaxB * (Hq + 2 * Hkv) * kD * 2;
+}
+constexpr size_t kStagingPosBytes = kMaxR * kMaxB * 8;
+__host__ __device__ constexpr size_t staging_bytes(int Hq, int Hkv) {
+    return staging_qkv_bytes(Hq, Hkv) + kStagingPosBytes + 64;
+}
 constexpr int kMaxPageStride = 0x7fffffff / kP;  // page_stride * 64 stays an int
 constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
@@ -544,7 +558,22 @@ __device__ __forceinline__ void tmem_st_h16(uint32_t taddr, const uint32_t (&r)[
 
 }  // namespace tc
 
-template <bool QKNORM>
+// Positions of the call's tokens lane and lane + 32 (row warps 1-3 keep
+// them in registers and share them by shuffle).
+__device__ __forceinline__ void load_positions(const Params &p, int lane, long long &pos_lo, long long &pos_hi) {
+    const int nt = p.R * p.B;
+    if (lane < nt)
+        pos_lo = p.pos_i64 ? reinterpret_cast<const long long *>(p.positions)[lane]
+                           : reinterpret_cast<const int *>(p.positions)[lane];
+    if (lane + 32 < nt)
+        pos_hi = p.pos_i64 ? reinterpret_cast<const long long *>(p.positions)[lane + 32]
+                           : reinterpret_cast<const int *>(p.positions)[lane + 32];
+}
+
+// STAGED: qkv and the positions come from the workspace copy that
+// k3da_stage_kernel (this grid's programmatic prerequisite) writes; the row
+// warps wait for it before their first read of either.
+template <bool QKNORM, bool STAGED>
 __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     k3da_tc_kernel(const __grid_constant__ CUtensorMap pool_map, const __grid_constant__ Params p) {
     using namespace tc;
@@ -577,19 +606,17 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     if (QKNORM && threadIdx.x < kRowThreads) {
         w_early = threadIdx.x < kD ? p.q_w[threadIdx.x] : p.k_w[threadIdx.x - kD];
         if (warp != 0) {
-            const int nt = p.R * p.B;
-            if (lane < nt)
-                pos_lo = p.pos_i64 ? reinterpret_cast<const long long *>(p.positions)[lane]
-                                   : reinterpret_cast<const int *>(p.positions)[lane];
-            if (lane + 32 < nt)
-                pos_hi = p.pos_i64 ? reinterpret_cast<const long long *>(p.positions)[lane + 32]
-                                   : reinterpret_cast<const int *>(p.positions)[lane + 32];
+            if (!STAGED) load_positions(p, lane, pos_lo, pos_hi);
 #pragma unroll
             for (int j = 0; j < kD / 2; ++j)
                 if (lane == j) my_rate = p.turn_rate[j];
         }
     }
     build_plan(p, pl, blockIdx.x, p.grid, blockIdx.x == 0);
+    if (STAGED && warp < kRowWarps) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (QKNORM && warp != 0) load_positions(p, lane, pos_lo, pos_hi);
+    }
     {
         // Q and block tiles start as zeros: rows without a query row or a
         // block token stay zero for the whole kernel.
@@ -1106,6 +1133,7 @@ constexpr int kCombineThreads = 64 * kCombineRows;  // (row, 8 dims, chunk lane)
 constexpr int kCombineLanes = 8;
 constexpr int kCombineFold = 2;
 
+template <bool STAGED>
 __global__ void __launch_bounds__(kCombineThreads, 768 / kCombineThreads) k3da_combine_kernel(const __grid_constant__ Params p) {
     const int per_unit = kRows / kCombineRows;
     const int u = blockIdx.x / per_unit;
@@ -1115,13 +1143,24 @@ __global__ void __launch_bounds__(kCombineThreads, 768 / kCombineThreads) k3da_c
     if ((blockIdx.x - u * per_unit) * kCombineRows >= rows) return;  // whole CTA
     const int r = u / p.Hkv, h = u - r * p.Hkv;
     bool bad;
-    const int L = clamped_length(p, __ldg(p.ctx_lens + r), &bad);
-    int ch, nch;
-    unit_chunking(1 + (L + kP - 1) / kP, p.splits, ch, nch);
+    // The lengths are an input: read before the wait, while the split pass
+    // still runs -- unless they were staged (STAGED: the wait then orders the
+    // read of the copy after the stage kernel, two grids back).
+    int ch = 1, nch = 0;
+    if (!STAGED)
+        unit_chunking(1 + (clamped_length(p, __ldg(p.ctx_lens + r), &bad) + kP - 1) / kP, p.splits, ch, nch);
     const uint8_t *slots = reinterpret_cast<const uint8_t *>(p.ws_o) +
                            static_cast<long long>(u) * p.slots_per_unit * kPartialElems * 2;
     const float2 *mls = p.ws_ml + static_cast<long long>(u) * p.slots_per_unit * kRows;
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (STAGED) {
+        // The staged lengths follow the partials, the qkv and the positions.
+        const int32_t *lens = reinterpret_cast<const int32_t *>(
+            reinterpret_cast<const uint8_t *>(p.ws_o) +
+            static_cast<long long>(p.R) * p.Hkv * p.slots_per_unit * kSlotBytes + staging_qkv_bytes(p.Hq, p.Hkv) +
+            kStagingPosBytes);
+        unit_chunking(1 + (clamped_length(p, lens[r], &bad) + kP - 1) / kP, p.splits, ch, nch);
+    }
     float m = -INFINITY, l = 0.f;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (row < rows) {
@@ -1186,6 +1225,40 @@ __global__ void __launch_bounds__(kCombineThreads, 768 / kCombineThreads) k3da_c
     }
 }
 
+// ----------------------------------------------------------------- stage --
+//
+// Host-resident inputs (pinned host memory the GPU addresses directly): the
+// split pass reads each unit's q and block rows in every CTA that holds one
+// of the unit's chunks, so read across the host link in place they would
+// cross it about ten times over.  This kernel copies qkv, the positions and
+// the lengths into the workspace once; the split pass is launched as its
+// programmatic dependent (its plan and setup overlap the copy, its row warps
+// wait for it) and reads the copies.  The page table is read in place: each
+// entry is read by one CTA only.
+struct StageParams {
+    const uint4 *qkv_src;
+    uint4 *qkv_dst;
+    long long qkv_vecs;  // 16-byte words of qkv
+    const int32_t *pos_src;
+    int32_t *pos_dst;
+    int pos_words;       // 4-byte words of the positions (0 for the plain variant)
+    const int32_t *lens_src;
+    int32_t *lens_dst;
+    int R;
+};
+constexpr int kStageThreads = 256;
+
+__global__ void __launch_bounds__(kStageThreads) k3da_stage_kernel(const __grid_constant__ StageParams s) {
+    // The split pass may start at once: only its row warps wait, in
+    // griddepcontrol.wait, for this grid to complete.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const long long stride = static_cast<long long>(gridDim.x) * kStageThreads;
+    const long long t = static_cast<long long>(blockIdx.x) * kStageThreads + threadIdx.x;
+    for (long long i = t; i < s.qkv_vecs; i += stride) s.qkv_dst[i] = s.qkv_src[i];
+    if (t < s.pos_words) s.pos_dst[t] = s.pos_src[t];
+    if (t < s.R) s.lens_dst[t] = s.lens_src[t];
+}
+
 // ------------------------------------------------------- wait self-test --
 //
 // Exercises the bounded wait every kernel of the library uses, on an
@@ -1212,8 +1285,11 @@ __global__ void __launch_bounds__(128) k3da_wait_selftest_kernel(int32_t *status
 
 constexpr int kSplitThreads = tc::kThreads;
 constexpr int kSplitSmem = tc::kSmemBytes;
-const void *const kSplitKernel[2] = {reinterpret_cast<const void *>(&k3da_tc_kernel<false>),
-                                     reinterpret_cast<const void *>(&k3da_tc_kernel<true>)};
+// Indexed by qknorm + 2 * staged.
+const void *const kSplitKernel[4] = {reinterpret_cast<const void *>(&k3da_tc_kernel<false, false>),
+                                     reinterpret_cast<const void *>(&k3da_tc_kernel<true, false>),
+                                     reinterpret_cast<const void *>(&k3da_tc_kernel<false, true>),
+                                     reinterpret_cast<const void *>(&k3da_tc_kernel<true, true>)};
 
 // CTAs of `kernel` that fit on one SM: registers (per-warp allocation in
 // units of 256), shared memory (with the per-block reservation), threads,
@@ -1300,8 +1376,8 @@ int configure_device(int dev, DeviceConfig *cfg) {
         d.ready = false;
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) rc = K3DA_ECUDA;
-        int occ[2] = {0, 0};
-        for (int v = 0; v < 2 && rc == K3DA_OK; ++v) {
+        int occ[4] = {0, 0, 0, 0};
+        for (int v = 0; v < 4 && rc == K3DA_OK; ++v) {
             // Ask for the largest shared-memory carveout, then size the grid
             // from the occupancy it allows.
             if (cudaFuncSetAttribute(kSplitKernel[v], cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem) !=
@@ -1313,10 +1389,12 @@ int configure_device(int dev, DeviceConfig *cfg) {
                 rc = occupancy_of(kSplitKernel[v], kSplitThreads, kSplitSmem, dev, &occ[v]);
         }
         if (rc == K3DA_OK && !driver_entry("cuTensorMapEncodeTiled", 12000, &g_encode)) rc = K3DA_ECUDA;
-        for (int v = 0; v < 2 && rc == K3DA_OK; ++v) {
+        for (int v = 0; v < 4 && rc == K3DA_OK; ++v) {
             if (occ[v] < 1) rc = K3DA_ECUDA;
             if (occ[v] > kMaxCtasPerSm) occ[v] = kMaxCtasPerSm;
         }
+        // The staged forms share their plain form's grid.
+        if (rc == K3DA_OK && (occ[2] != occ[0] || occ[3] != occ[1])) rc = K3DA_ECUDA;
         if (rc == K3DA_OK) {
             d.sms = sms;
             d.occupancy[0] = occ[0];
@@ -1346,11 +1424,20 @@ constexpr size_t workspace_slots(int R, int Hkv, int page_stride) {
     return static_cast<size_t>(R) * Hkv * static_cast<size_t>(slots_per_unit(R, Hkv, page_stride));
 }
 
-constexpr size_t kWsHeaderBytes = 512;  // reserved; the partials follow (16-byte aligned, as the workspace is)
-constexpr size_t kSlotBytes = kPartialElems * 2 + kRows * 8;  // bf16 O, then (m, l) fp32 per row
-
 constexpr size_t workspace_for(int R, int Hkv, int page_stride) {
     return kWsHeaderBytes + workspace_slots(R, Hkv, page_stride) * kSlotBytes;
+}
+
+// Pinned host memory (allocated or registered with CUDA) that kernels
+// address directly.  Anything else -- device memory, managed memory, a
+// pointer CUDA does not know -- is read in place.
+bool host_resident(const void *ptr) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        cudaGetLastError();  // clear the error of an unknown pointer
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
 }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -1399,7 +1486,7 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
            float softmax_scale, bool qknorm, const void *positions, int pos_dtype, const void *q_norm_w,
            const void *k_norm_w, float eps, float rope_base, const k3da_yarn *yarn, void *workspace,
            size_t workspace_bytes,
-           int32_t *status, void *stream) {
+           int32_t *status, void *stream, bool staging_optional = false) {
     if (!out || !qkv || !kv_pool || !page_table || !ctx_lens) return K3DA_EINVAL;
     if (!aligned(out, 16) || !aligned(qkv, 16) || !aligned(kv_pool, 16) || !aligned(page_table, 4) ||
         !aligned(ctx_lens, 4) || (status && !aligned(status, 4)))
@@ -1425,7 +1512,12 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
     DeviceConfig cfg;
     int rc = configure_device(dev, &cfg);
     if (rc != K3DA_OK) return rc;
-    if (workspace_bytes < workspace_for(R, Hkv, page_stride)) return K3DA_EWORKSPACE;
+    const size_t ws_partials = workspace_for(R, Hkv, page_stride);
+    if (workspace_bytes < ws_partials + (staging_optional ? 0 : staging_bytes(Hq, Hkv))) return K3DA_EWORKSPACE;
+    // Host-resident qkv, positions or lengths are staged into the workspace
+    // by one small kernel first (where it has the room).
+    const bool staged = workspace_bytes >= ws_partials + staging_bytes(Hq, Hkv) &&
+                        (host_resident(qkv) || host_resident(ctx_lens) || (qknorm && host_resident(positions)));
 
     CUtensorMap map;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD),
@@ -1460,6 +1552,26 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
     prm.Hq = Hq;
     prm.Hkv = Hkv;
     prm.pos_i64 = pos_dtype == K3DA_POS_I64;
+    StageParams sp;
+    memset(&sp, 0, sizeof sp);
+    if (staged) {
+        uint8_t *base = static_cast<uint8_t *>(workspace) + ws_partials;
+        const long long qkv_bytes = static_cast<long long>(R) * B * (Hq + 2 * Hkv) * kD * 2;
+        sp.qkv_src = static_cast<const uint4 *>(qkv);
+        sp.qkv_dst = reinterpret_cast<uint4 *>(base);
+        sp.qkv_vecs = qkv_bytes / 16;
+        sp.pos_src = static_cast<const int32_t *>(positions);
+        sp.pos_dst = reinterpret_cast<int32_t *>(base + staging_qkv_bytes(Hq, Hkv));
+        sp.pos_words = qknorm ? R * B * (pos_dtype == K3DA_POS_I64 ? 2 : 1) : 0;
+        sp.lens_src = ctx_lens;
+        sp.lens_dst = reinterpret_cast<int32_t *>(base + staging_qkv_bytes(Hq, Hkv) + kStagingPosBytes);
+        sp.R = R;
+        // The split pass reads qkv and the positions from the copies; its
+        // plan reads ctx_lens in place (one small read per CTA, before the
+        // copy is done) and the combine reads the lengths' copy.
+        prm.qkv = reinterpret_cast<const __nv_bfloat16 *>(sp.qkv_dst);
+        if (qknorm) prm.positions = sp.pos_dst;
+    }
     const int occ = cfg.occupancy[qknorm ? 1 : 0];
     prm.grid = cfg.sms * occ;
     prm.scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -1472,10 +1584,30 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
     prm.rope_mscale = yarn != nullptr ? k3da_host::yarn_mscale(yarn) : 1.0f;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (qknorm)
-        k3da_tc_kernel<true><<<prm.grid, kSplitThreads, kSplitSmem, st>>>(map, prm);
-    else
-        k3da_tc_kernel<false><<<prm.grid, kSplitThreads, kSplitSmem, st>>>(map, prm);
+    if (staged) {
+        // Stage kernel, then the split pass as its programmatic dependent.
+        const long long blocks = (sp.qkv_vecs + kStageThreads - 1) / kStageThreads;
+        k3da_stage_kernel<<<static_cast<unsigned>(blocks < 1 ? 1 : blocks), kStageThreads, 0, st>>>(sp);
+        if (cudaGetLastError() != cudaSuccess) return K3DA_ECUDA;
+        cudaLaunchConfig_t sc;
+        memset(&sc, 0, sizeof sc);
+        sc.gridDim = dim3(static_cast<unsigned>(prm.grid));
+        sc.blockDim = dim3(kSplitThreads);
+        sc.dynamicSmemBytes = kSplitSmem;
+        sc.stream = st;
+        cudaLaunchAttribute sa[1];
+        sa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        sa[0].val.programmaticStreamSerializationAllowed = 1;
+        sc.attrs = sa;
+        sc.numAttrs = 1;
+        const cudaError_t e = qknorm ? cudaLaunchKernelEx(&sc, k3da_tc_kernel<true, true>, map, prm)
+                                     : cudaLaunchKernelEx(&sc, k3da_tc_kernel<false, true>, map, prm);
+        if (e != cudaSuccess) return K3DA_ECUDA;
+    } else if (qknorm) {
+        k3da_tc_kernel<true, false><<<prm.grid, kSplitThreads, kSplitSmem, st>>>(map, prm);
+    } else {
+        k3da_tc_kernel<false, false><<<prm.grid, kSplitThreads, kSplitSmem, st>>>(map, prm);
+    }
     if (cudaGetLastError() != cudaSuccess) return K3DA_ECUDA;
     if (g_phase_event && cudaEventRecord(g_phase_event, st) != cudaSuccess) return K3DA_ECUDA;
     // The combine is a programmatic dependent of the split pass, so its
@@ -1491,7 +1623,9 @@ int launch(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, c
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    if (cudaLaunchKernelEx(&lc, k3da_combine_kernel, prm) != cudaSuccess) return K3DA_ECUDA;
+    if (cudaLaunchKernelEx(&lc, staged ? k3da_combine_kernel<true> : k3da_combine_kernel<false>, prm) !=
+        cudaSuccess)
+        return K3DA_ECUDA;
     if (cudaGetLastError() != cudaSuccess) return K3DA_ECUDA;
     return K3DA_OK;
 }
@@ -1505,7 +1639,7 @@ size_t k3da_workspace_bytes(int num_requests, int block_len, int num_q_heads, in
     if (num_requests < 1 || num_requests > kMaxR || block_len < 1 || block_len > kMaxB ||
         !supported_heads(num_q_heads, num_kv_heads) || page_stride < 1 || page_stride > kMaxPageStride)
         return 0;
-    return workspace_for(num_requests, num_kv_heads, page_stride);
+    return workspace_for(num_requests, num_kv_heads, page_stride) + staging_bytes(num_q_heads, num_kv_heads);
 }
 
 int k3da_attn(void *out, const void *qkv, const void *kv_pool, int64_t num_pages, const int32_t *page_table,
@@ -1555,7 +1689,8 @@ int k3da_attn_qknorm_noalloc(void *out, const void *qkv, const void *kv_pool, in
     if (rc != K3DA_OK) return rc;
     return launch(out, qkv, kv_pool, num_pages, page_table, page_stride, ctx_lens, num_requests, block_len,
                   num_q_heads, num_kv_heads, head_dim, softmax_scale, true, positions, pos_dtype, q_norm_w,
-                  k_norm_w, eps, rope_base, nullptr, scratch, kStaticScratchBytes, status, stream);
+                  k_norm_w, eps, rope_base, nullptr, scratch, kStaticScratchBytes, status, stream,
+                  /*staging_optional=*/true);
 }
 
 size_t k3da_noalloc_scratch_bytes(void) { return kStaticScratchBytes; }

@@ -1,6 +1,7 @@
-"""Inputs and output in pinned host memory: the kernels read qkv, the page
-table, the lengths and the positions, and write the output, across the host
-link with no separate copy.  The result must equal the call on
+"""Inputs and output in pinned host memory: a stage kernel copies qkv, the
+positions and the lengths into the workspace across the host link, the split
+pass reads the page table in place, and the combine writes the output to host
+memory; no cudaMemcpy is involved.  The result must equal the call on
 device-resident copies of the same tensors bit for bit (the same kernels run
 on the same values), and a captured call must pick up host buffers rewritten
 between replays."""
@@ -52,6 +53,22 @@ def test_host_inputs_equal_device_inputs_bit_for_bit(config):
     assert torch.equal(out.view(torch.int16), dev_out.cpu().view(torch.int16))
     if config in ("tiny", "mixed_8x8"):
         assert_close(out.cuda(), oracle_for(case), f"{config} from host memory")
+
+
+@pytest.mark.parametrize("which", ["qkv", "page_table", "ctx_lens", "positions", "out"])
+def test_each_tensor_alone_in_host_memory(which):
+    """One tensor host-resident, the rest on the device (qkv, positions or
+    lengths alone still take the staged path); int64 positions, strided
+    page-table rows."""
+    case = workloads.heads_24_4(device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = k3da.run_case(case, status=status)
+    c = case if which == "out" else dataclasses.replace(case, **{which: pinned(getattr(case, which))})
+    out = host_out(case) if which == "out" else torch.empty_like(ref)
+    k3da.run_case(c, out=out, workspace=k3da.case_workspace(case), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(out.cpu().view(torch.int16), ref.cpu().view(torch.int16))
 
 
 def test_graph_replay_reads_rewritten_host_buffers():

@@ -9,8 +9,9 @@ k3da_attn_qknorm with a caller-owned workspace (the same kernels on the same
 inputs, and reruns are bitwise), and to match the oracle element by element
 (2e-2 absolute + 2e-2 relative).  Calls come in a row with other inputs and
 other shapes in between, so stale scratch contents would show.  Sizes beyond
-the array are refused.  Kept in the last test file so a run that stops at the
-first failure has already run every other test."""
+the array are refused.  Host-resident inputs work through it too.  Kept in
+the last test file so a run that stops at the first failure has already run
+every other test."""
 import pytest
 import torch
 
@@ -57,12 +58,43 @@ def test_noalloc_matches_the_workspace_entry_point_twice(maker):
         assert_close(got, oracle_for(case), f"no-allocation seed {seed}")
 
 
+def stride_case(stride, seed=23):
+    return workloads.build_case(f"stride{stride}", R=8, B=8, Hq=24, Hkv=4, lens=[64] * 8, page_stride=stride,
+                                used_per_row=1, num_pages=16, qknorm=True, seed=seed, device="cuda")
+
+
 def test_noalloc_refuses_sizes_beyond_its_scratch():
-    lib = k3da.load_library()
-    cap = lib.k3da_noalloc_scratch_bytes()
-    assert lib.k3da_workspace_bytes(8, 8, 24, 4, 1279) <= cap < lib.k3da_workspace_bytes(8, 8, 24, 4, 1280)
-    assert lib.k3da_workspace_bytes(8, 8, 24, 4, 2048) > cap
-    case = workloads.build_case("big", R=8, B=8, Hq=24, Hkv=4, lens=[64] * 8, page_stride=2048,
-                                used_per_row=1, num_pages=16, qknorm=True, seed=23, device="cuda")
-    with pytest.raises(k3da.K3daError):
-        without_allocation(case, None)
+    # The bound follows the chunk partials alone (the staging room that
+    # k3da_workspace_bytes adds is optional here): page_stride 1279 runs,
+    # 1280 and 2048 are refused.
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    case = stride_case(1279)
+    got = without_allocation(case, status)
+    ref = with_workspace(case)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(bits(got), bits(ref))
+    for stride in (1280, 2048):
+        with pytest.raises(k3da.K3daError):
+            without_allocation(stride_case(stride), None)
+
+
+def pinned(t):
+    return t.cpu().contiguous().pin_memory()
+
+
+@pytest.mark.parametrize("stride", [40, 1279])
+def test_noalloc_with_host_resident_inputs(stride):
+    """Inputs and output in pinned host memory: staged through the scratch
+    where it has room (page_stride 40), read in place where it has not
+    (1279, whose partials nearly fill it); bitwise the device-input call."""
+    case = workloads.heads_24_4(device="cuda") if stride == 40 else stride_case(1279, seed=24)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full((case.T, case.Hq * case.D), float("nan"), dtype=torch.bfloat16).pin_memory()
+    k3da.k3da_attn_qknorm_noalloc(out, pinned(case.qkv), case.pool, pinned(case.page_table),
+                                  pinned(case.ctx_lens), pinned(case.positions), case.q_norm_w, case.k_norm_w,
+                                  block_len=case.B, num_q_heads=case.Hq, num_kv_heads=case.Hkv, status=status)
+    ref = with_workspace(case)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(bits(out), bits(ref).cpu())

@@ -1116,29 +1116,30 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
 
 // --------------------------------------------------------------- combine --
 //
-// One CTA per (unit, 2 query rows), 128 threads: thread = (row, 8 dims,
-// chunk lane sg of 8), the 8 chunk lanes of one (row, dims) adjacent in a
-// warp.  Lane sg folds the unit's chunk partials sg, sg+8, ... online; it
-// issues the loads of kCombineFold of them at once (deeper folds measured
-// slower on the 8x8 workloads and no faster on long contexts); the lanes
-// then merge by a fixed
-// butterfly of shuffles, so the result depends on nothing but the unit's own
-// chunks.  Launched as a programmatic dependent of the split pass: the
-// unit's chunk count comes from its context length (an input, read before
-// griddepcontrol.wait while the split pass still runs), its partials sit at
-// fixed slots, and griddepcontrol.wait orders every workspace read after
-// the split pass.
-constexpr int kCombineRows = 2;
-constexpr int kCombineThreads = 64 * kCombineRows;  // (row, 8 dims, chunk lane) per thread
-constexpr int kCombineLanes = 8;
-constexpr int kCombineFold = 2;
+// One CTA per (unit, 4 query rows), 128 threads: thread = (row, 8 dims,
+// chunk lane sg of 4), the 4 chunk lanes of one (row, dims) adjacent in a
+// warp.  Lane sg folds the unit's chunk partials sg, sg+4, ... online,
+// issuing the loads of kCombineFold of them at once; the lanes then merge by
+// a fixed butterfly of shuffles, so the result depends on nothing but the
+// unit's own chunks.  (Of 1, 2, 4, 8 and 16 lanes with folds of 1 to 8, 4
+// lanes folding 4 at a time measured fastest on every workload.)  Launched
+// as a programmatic dependent of the split pass: the unit's chunk count
+// comes from its context length (an input, read before griddepcontrol.wait
+// while the split pass still runs), its partials sit at fixed slots, and
+// griddepcontrol.wait orders every workspace read after the split pass.
+constexpr int kCombineRows = 4;
+constexpr int kCombineLanes = 4;
+constexpr int kCombineThreads = 8 * kCombineLanes * kCombineRows;  // (row, 8 dims, chunk lane) per thread
+constexpr int kCombineFold = 4;
+static_assert(kRows % kCombineRows == 0 && (kCombineLanes & (kCombineLanes - 1)) == 0 && kCombineLanes <= 32,
+              "whole rows per CTA; a row's chunk lanes are adjacent lanes of one warp");
 
 template <bool STAGED>
 __global__ void __launch_bounds__(kCombineThreads, 768 / kCombineThreads) k3da_combine_kernel(const __grid_constant__ Params p) {
     const int per_unit = kRows / kCombineRows;
     const int u = blockIdx.x / per_unit;
-    const int row = (blockIdx.x - u * per_unit) * kCombineRows + (threadIdx.x >> 6);
-    const int dc = (threadIdx.x >> 3) & 7, sg = threadIdx.x & (kCombineLanes - 1);
+    const int row = (blockIdx.x - u * per_unit) * kCombineRows + threadIdx.x / (8 * kCombineLanes);
+    const int dc = (threadIdx.x / kCombineLanes) & 7, sg = threadIdx.x & (kCombineLanes - 1);
     const int rows = kG * p.B;
     if ((blockIdx.x - u * per_unit) * kCombineRows >= rows) return;  // whole CTA
     const int r = u / p.Hkv, h = u - r * p.Hkv;

@@ -43,6 +43,10 @@
 //   * Each chunk leaves an unnormalised partial (O as bf16, m and l in fp32)
 //     in the workspace; the combine kernel folds a unit's chunk partials in
 //     a fixed order and writes bf16 out, so reruns are bit-identical.
+//   * Inputs and output may be pinned host memory the GPU addresses across
+//     the host link.  Then a stage kernel first copies qkv, positions and
+//     lengths into the workspace, once, and the split pass (its
+//     programmatic dependent) reads the copies.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>

@@ -259,9 +259,10 @@ int k3da_attn_qknorm_yarn(void *out, const void *qkv, const void *kv_pool, int64
  * dims of a head; RoPE turns the pairs (j, j+32) by positions[t] *
  * rope_base^(-2j/64).  It is the transform k3da_attn_qknorm applies to the
  * block's q and k before attending, exported for the step that writes new
- * K into the pool.
+ * K into the pool.  It rounds exactly as k3da_attn_qknorm does, so this call
+ * followed by k3da_attn gives k3da_attn_qknorm's output bit for bit.
  *
- *   qkv          [T, (Hq + 2*Hkv)*64] bf16, read and written.  2-byte aligned.
+ *   qkv          [T, (Hq + 2*Hkv)*64] bf16, read and written.  16-byte aligned.
  *   num_tokens   T >= 1 (the drafter runs 1..64).
  *   num_q_heads, num_kv_heads   (6, 1) or (24, 4);  head_dim 64.
  *   positions    [T] int32 or int64 (pos_dtype), aligned to its type.

@@ -926,7 +926,8 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                         const float half_turns = static_cast<float>(static_cast<int>(turns >> 32)) * 0x1p-31f;
                         float sn, cs;
                         sincospif(half_turns, &sn, &cs);
-                        trig[(e & 31) * kTrigStride + (e >> 5)] = make_float2(cs * p.rope_mscale, sn * p.rope_mscale);
+                        trig[(e & 31) * kTrigStride + (e >> 5)] =
+                            make_float2(__fmul_rn(cs, p.rope_mscale), __fmul_rn(sn, p.rope_mscale));
                     }
                 }
             }
@@ -956,18 +957,21 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
                 }
                 float ss = 0.f;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) ss = fmaf(lo[e], lo[e], fmaf(hi[e], hi[e], ss));
-                ss += __shfl_xor_sync(kFull, ss, 1);
+                for (int e = 0; e < 16; ++e) ss = __fmaf_rn(lo[e], lo[e], __fmaf_rn(hi[e], hi[e], ss));
+                ss = __fadd_rn(ss, __shfl_xor_sync(kFull, ss, 1));
                 if (norm) {
-                    const float inv = rsqrtf(ss * (1.0f / kD) + p.eps);
+                    // Rounding pinned operation by operation (the standalone
+                    // norm+RoPE call does exactly the same, so it followed by
+                    // the plain attention gives this call's bits).
+                    const float inv = rsqrtf(__fmaf_rn(ss, 1.0f / kD, p.eps));
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const int jp = 16 * hp + e;
-                        const float n_lo = lo[e] * inv * __bfloat162float(w[jp]);
-                        const float n_hi = hi[e] * inv * __bfloat162float(w[jp + 32]);
+                        const float n_lo = __fmul_rn(__fmul_rn(lo[e], inv), __bfloat162float(w[jp]));
+                        const float n_hi = __fmul_rn(__fmul_rn(hi[e], inv), __bfloat162float(w[jp + 32]));
                         const float2 cs = trig[jp * kTrigStride + ti];
-                        lo[e] = n_lo * cs.x - n_hi * cs.y;
-                        hi[e] = n_hi * cs.x + n_lo * cs.y;
+                        lo[e] = __fmaf_rn(n_lo, cs.x, -__fmul_rn(n_hi, cs.y));
+                        hi[e] = __fmaf_rn(n_hi, cs.x, __fmul_rn(n_lo, cs.y));
                     }
                 }
                 if (dst != nullptr) {

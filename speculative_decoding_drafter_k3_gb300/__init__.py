@@ -268,7 +268,7 @@ def alloc_workspace(num_requests: int, block_len: int, num_q_heads: int, num_kv_
 
 
 def case_workspace(case) -> torch.Tensor:
-    return alloc_workspace(case.R, case.B, case.Hq, case.Hkv, case.page_stride, case.qkv.device)
+    return alloc_workspace(case.R, case.B, case.Hq, case.Hkv, case.page_stride, case.pool.device)
 
 
 def run_case(case, out=None, workspace=None, status=None, stream=None, yarn=None):
@@ -276,7 +276,7 @@ def run_case(case, out=None, workspace=None, status=None, stream=None, yarn=None
     the GPU; its qkv, page table, lengths and positions may be pinned host
     tensors (``yarn``: YaRN RoPE for the fused variant)."""
     if out is None:
-        out = torch.empty(case.T, case.Hq * case.D, dtype=torch.bfloat16, device=case.qkv.device)
+        out = torch.empty(case.T, case.Hq * case.D, dtype=torch.bfloat16, device=case.pool.device)
     if workspace is None:
         workspace = case_workspace(case)
     kw = dict(block_len=case.B, num_q_heads=case.Hq, num_kv_heads=case.Hkv,

@@ -8,6 +8,7 @@ rewritten lengths, page table, qkv and positions.  Reruns, the pool and
 graph replay are checked on every workload of the op: the tiny plain call,
 the 8x8 mixed-length and 24/4 strided cases, all eight request x token
 splits and the long-context stress case."""
+import dataclasses
 import functools
 
 import numpy as np
@@ -199,3 +200,33 @@ def test_a_stuck_wait_times_out_with_a_status_and_the_context_survives():
 def ctypes_ptr(t):
     import ctypes
     return ctypes.c_void_p(t.data_ptr())
+
+
+def test_calls_on_concurrent_streams_with_their_own_workspaces():
+    """The library keeps no per-call state: calls in flight at the same time
+    on different streams, each with its own workspace (one of them with
+    host-resident inputs), give the bits of the same calls made one after
+    the other."""
+    makers = [workloads.mixed_8x8, workloads.heads_24_4, workloads.w6_8x6,
+              functools.partial(workloads.split_sweep, 3, 5)]
+    cases = [m(device="cuda") for m in makers]
+    seq = [k3da.run_case(c).clone() for c in cases]
+    torch.cuda.synchronize()
+    host = cases[1]
+    pinned = lambda t: t.cpu().contiguous().pin_memory()
+    cases[1] = dataclasses.replace(host, qkv=pinned(host.qkv), page_table=pinned(host.page_table),
+                                   ctx_lens=pinned(host.ctx_lens), positions=pinned(host.positions))
+    streams = [torch.cuda.Stream() for _ in cases]
+    wss = [k3da.case_workspace(c) for c in cases]
+    outs = [fresh_out(c) for c in cases]
+    status = [torch.zeros(1, dtype=torch.int32, device="cuda") for _ in cases]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for c, s, w, o, st in zip(cases, streams, wss, outs, status):
+            with torch.cuda.stream(s):
+                o.fill_(float("nan"))
+                k3da.run_case(c, out=o, workspace=w, status=st, stream=s)
+        torch.cuda.synchronize()
+        for o, ref, st in zip(outs, seq, status):
+            assert int(st.item()) == 0
+            assert torch.equal(o.view(torch.int16), ref.view(torch.int16))

@@ -22,6 +22,7 @@ CONFIGS = {
     "heads_24_4": workloads.heads_24_4,
     "w6_8x6": workloads.w6_8x6,
     "long_context_small": workloads.long_context_small,
+    "long_context": workloads.long_context,
 }
 
 
